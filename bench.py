@@ -1,0 +1,625 @@
+"""Benchmark of the FP8 block-scaled linear on one GB300 (or N replicas).
+
+Workload of the headline line: DeepSeek-V3 decode-shaped linears at batch
+M=16 tokens -- wq_a (7168->1536), wq_b (1536->24576), wo (16384->7168) --
+with bf16 activations ~N(0,1) (0.5% outliers x30) and e4m3 weights with
+128x128 fp32 block scales drawn from N(0, 0.02).  One step = act_quant +
+fp8_gemm for each of the three layers (6 kernel launches), replayed from CUDA
+graphs.  Four weight sets (4 x 167 MB) rotate between steps so every step
+streams its weights from HBM (inputs larger than L2).
+
+value  = algorithmic HBM bytes of the step / device time (GB/s); the
+         algorithmic bytes are what the method must move (weights + their
+         scales, activations in, codes/scales out and back in, outputs);
+e2e    = same metric through the Python binding with host buffers: each
+         step copies the activations host->device, runs the six calls and
+         copies the outputs device->host;
+roofline = the fp8_gemm kernel alone (the dominant kernel), per-launch
+         CUDA-event durations taken inside the timed graphs;
+cpu_baseline = the CPU oracle on the host cores over a bounded sample.
+
+With --impl reference the CPU oracle itself is timed on the same workload
+(each step a bounded sample: all three layers' act_quant and 1/16 of each
+layer's output features).  Under torchrun each rank runs an independent
+replica (the method has no exchange step); rank 0 prints the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic as syn  # noqa: E402
+
+M_DECODE = 16
+ROTATIONS = 4
+LAYERS = list(syn.DECODE_LAYERS)      # wq_a, wq_b, wo
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ accounting
+def act_quant_bytes(M, K):
+    return M * K * 2 + M * K + 4 * M * (K // 128)
+
+
+def gemm_bytes(M, N, K):
+    nb, kb = (N + 127) // 128, K // 128
+    return N * K + 4 * nb * kb + M * K + 4 * M * kb + 2 * M * N
+
+
+def gemm_flops(M, N, K):
+    return 2 * M * N * K
+
+
+def decode_step_bytes(M):
+    return sum(act_quant_bytes(M, K) + gemm_bytes(M, N, K) for N, K in syn.DECODE_LAYERS.values())
+
+
+def decode_step_flops(M):
+    return sum(gemm_flops(M, N, K) for N, K in syn.DECODE_LAYERS.values())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "fp8_block_scaled_07_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, interval_ms=20):
+        self.index, self.interval_ms = index, interval_ms
+        self.proc, self.lines, self.t0, self.t1 = None, [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._th = threading.Thread(target=self._read, daemon=True)
+            self._th.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 is None or (self.t0 - 0.03 <= t <= self.t1 + 0.03)]
+        if not rows:
+            rows = [l for (_, l) in self.lines[-3:]]
+        sm, smax, reasons = [], None, set()
+        for l in rows:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ decode workload
+class Decode:
+    def __init__(self, fp8, torch, M=M_DECODE, rotations=ROTATIONS, seed=syn.SEED_BASE + 1):
+        self.fp8, self.torch, self.M, self.R = fp8, torch, M, rotations
+        dev = torch.device("cuda")
+        self.w, self.x, self.xq, self.xs, self.y = [], [], {}, {}, {}
+        for r in range(rotations):
+            wr, xr = {}, {}
+            for i, name in enumerate(LAYERS):
+                N, K = syn.DECODE_LAYERS[name]
+                wb = syn.normal_bf16_device((N, K), 0.02, seed * 1000 + r * 10 + i, dev)
+                wr[name] = fp8.fp8_weight_quant(wb)
+                del wb
+                xr[name] = syn.normal_bf16_device((M, K), 1.0, seed * 1000 + 500 + r * 10 + i, dev,
+                                                  outlier_frac=0.005, outlier_mult=30.0)
+            self.w.append(wr)
+            self.x.append(xr)
+        for name in LAYERS:
+            N, K = syn.DECODE_LAYERS[name]
+            self.xq[name] = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+            self.xs[name] = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+            self.y[name] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        need = max(fp8.fp8_gemm_workspace_size(M, *syn.DECODE_LAYERS[n]) for n in LAYERS)
+        self.ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def step(self, r, x=None, events=None):
+        fp8 = self.fp8
+        xs = self.x[r] if x is None else x
+        for i, name in enumerate(LAYERS):
+            wq, wsc = self.w[r][name]
+            fp8.fp8_act_quant(xs[name], y=self.xq[name], s=self.xs[name])
+            if events is not None:
+                events[i][0].record()
+            fp8.fp8_gemm(self.xq[name], self.xs[name], wq, wsc, c_bf16=self.y[name], workspace=self.ws)
+            if events is not None:
+                events[i][1].record()
+
+
+def make_event(torch, external):
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=True)
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()                      # eager warm-up (attributes, tensor maps)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+# ------------------------------------------------------------------ CPU baseline
+def oracle_decode_sample(torch, dec, fraction_den, rotation=0):
+    """Oracle act_quant of all three inputs + GEMM over 1/fraction_den of
+    each layer's output features.  Returns (seconds, bytes, flops)."""
+    import oracle
+    inputs = []
+    for name in LAYERS:
+        N, K = syn.DECODE_LAYERS[name]
+        wq, ws = dec.w[rotation][name]
+        n_s = max(128, (N // fraction_den) // 128 * 128)
+        wq_h = wq[:n_s].contiguous().cpu().view(torch.uint8).numpy()
+        ws_h = ws[: n_s // 128].contiguous().cpu().numpy()
+        x_h = dec.x[rotation][name].cpu().view(torch.int16).numpy().view(np.uint16)
+        inputs.append((x_h, wq_h, ws_h, n_s, K))
+    oracle.lib()
+    t0 = time.perf_counter()
+    nbytes = flops = 0
+    for x_h, wq_h, ws_h, n_s, K in inputs:
+        aq, as_ = oracle.act_quant(x_h)
+        oracle.gemm(aq, as_, wq_h, ws_h)
+        nbytes += act_quant_bytes(dec.M, K) + gemm_bytes(dec.M, n_s, K)
+        flops += gemm_flops(dec.M, n_s, K)
+    return time.perf_counter() - t0, nbytes, flops
+
+
+def omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v and v.isdigit() else (os.cpu_count() or 1)
+
+
+# ------------------------------------------------------------------ per-row measurements
+def time_graph(torch, g, iters):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g.replay()
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(iters):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def rows_measurements(fp8, torch, peaks):
+    """Every other hot-path row on its own workload (device time)."""
+    dev = torch.device("cuda")
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = 2.0 * peaks["bf16_tflops"]           # dense fp8 = 2x dense bf16 (nominal ratio)
+    out = {}
+
+    # act_quant alone, prefill-sized input larger than L2 (4096 x 18432 bf16 = 151 MB)
+    xa = [syn.normal_bf16_device((4096, 18432), 1.0, 77 + i, dev) for i in range(2)]
+    ya = torch.empty((4096, 18432), dtype=torch.float8_e4m3fn, device=dev)
+    sa = torch.empty((4096, 144), dtype=torch.float32, device=dev)
+    gs = [capture(torch, lambda i=i: fp8.fp8_act_quant(xa[i], y=ya, s=sa)) for i in range(2)]
+    ms = sum(time_graph(torch, g, 20) for g in gs) / 2
+    b = act_quant_bytes(4096, 18432)
+    out["act_quant"] = {"workload": "4096x18432 bf16", "us": ms * 1e3, "GB/s": b / ms / 1e6,
+                        "frac_hbm": b / ms / 1e6 / hbm}
+    del xa, ya, sa, gs
+
+    # weight_dequant 18432 x 7168
+    w = syn.normal_bf16_device((18432, 7168), 0.02, 78, dev)
+    wq, ws = fp8.fp8_weight_quant(w)
+    del w
+    yd = torch.empty((18432, 7168), dtype=torch.bfloat16, device=dev)
+    g = capture(torch, lambda: fp8.fp8_weight_dequant(wq, ws, y=yd))
+    ms = time_graph(torch, g, 20)
+    b = 18432 * 7168 * 3 + 4 * 144 * 56
+    out["weight_dequant"] = {"workload": "18432x7168 e4m3 -> bf16", "us": ms * 1e3, "GB/s": b / ms / 1e6,
+                             "frac_hbm": b / ms / 1e6 / hbm}
+    del wq, ws, yd, g
+
+    # ragged wkv_a 7168 -> 576 with ue8m0 activations, M = 37 and 2049 (48 weight copies > L2)
+    for M in (37, 2049):
+        copies = 48 if M == 37 else 8
+        wk = [fp8.fp8_weight_quant(syn.normal_bf16_device(syn.WKV_A, 0.02, 900 + i, dev)) for i in range(copies)]
+        x = syn.normal_bf16_device((M, 7168), 1.0, 950 + M, dev)
+        xq = torch.empty((M, 7168), dtype=torch.float8_e4m3fn, device=dev)
+        xs = torch.empty((M, 56), dtype=torch.float32, device=dev)
+        y = torch.empty((M, 576), dtype=torch.bfloat16, device=dev)
+        wsb = torch.zeros(max(fp8.fp8_gemm_workspace_size(M, 576, 7168), 1), dtype=torch.uint8, device=dev)
+
+        def run():
+            for i in range(copies):
+                fp8.fp8_act_quant(x, fp8.FP8_SCALE_UE8M0, y=xq, s=xs)
+                fp8.fp8_gemm(xq, xs, wk[i][0], wk[i][1], c_bf16=y, workspace=wsb)
+        g = capture(torch, run)
+        ms = time_graph(torch, g, 5) / copies
+        b = act_quant_bytes(M, 7168) + gemm_bytes(M, 576, 7168)
+        f = gemm_flops(M, 576, 7168)
+        out[f"ragged_ue8m0_M{M}"] = {"workload": f"wkv_a 7168->576 M={M} ue8m0", "us": ms * 1e3,
+                                     "GB/s": b / ms / 1e6, "TFLOP/s": f / ms / 1e9}
+        del wk, g
+
+    # prefill dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2
+    M, D, I = 4096, syn.MLP_DIM, syn.MLP_INTER
+    w13q = torch.empty((2 * I, D), dtype=torch.float8_e4m3fn, device=dev)
+    w13s = torch.empty((2 * I // 128, D // 128), dtype=torch.float32, device=dev)
+    fp8.fp8_weight_quant(syn.normal_bf16_device((I, D), 0.02, 1, dev), q=w13q[:I], s=w13s[: I // 128])
+    fp8.fp8_weight_quant(syn.normal_bf16_device((I, D), 0.02, 2, dev), q=w13q[I:], s=w13s[I // 128:])
+    w2q, w2s = fp8.fp8_weight_quant(syn.normal_bf16_device((D, I), 0.02, 3, dev))
+    x = syn.normal_bf16_device((M, D), 1.0, 4, dev)
+    xq = torch.empty((M, D), dtype=torch.float8_e4m3fn, device=dev)
+    xs = torch.empty((M, D // 128), dtype=torch.float32, device=dev)
+    h13 = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=dev)
+    gq = torch.empty((M, I), dtype=torch.float8_e4m3fn, device=dev)
+    gsc = torch.empty((M, I // 128), dtype=torch.float32, device=dev)
+    yv = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+    ev = [make_event(torch, True) for _ in range(4)]
+    ext = all(e is not None for e in ev)
+
+    def mlp():
+        fp8.fp8_act_quant(x, y=xq, s=xs)
+        if ext:
+            ev[0].record()
+        fp8.fp8_gemm(xq, xs, w13q, w13s, c_bf16=h13)
+        if ext:
+            ev[1].record()
+        fp8.fp8_silu_mul_quant(h13, h13[:, I:], 2 * I, M, I, y=gq, s=gsc)
+        if ext:
+            ev[2].record()
+        fp8.fp8_gemm(gq, gsc, w2q, w2s, c_bf16=yv)
+        if ext:
+            ev[3].record()
+    g = capture(torch, mlp)
+    ms = time_graph(torch, g, 10)
+    flops = 3 * gemm_flops(M, I, D)
+    row = {"workload": "dense MLP M=4096, 7168->2x18432->7168", "ms": ms, "TFLOP/s": flops / ms / 1e9,
+           "frac_fp8_peak": flops / ms / 1e9 / fp8_peak}
+    if ext:
+        g.replay()
+        torch.cuda.synchronize()
+        t13, t2 = ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])
+        f13, f2 = gemm_flops(M, 2 * I, D), gemm_flops(M, D, I)
+        row["gemm_w13"] = {"ms": t13, "TFLOP/s": f13 / t13 / 1e9, "frac_fp8_peak": f13 / t13 / 1e9 / fp8_peak}
+        row["gemm_w2"] = {"ms": t2, "TFLOP/s": f2 / t2 / 1e9, "frac_fp8_peak": f2 / t2 / 1e9 / fp8_peak}
+    out["prefill_mlp"] = row
+    del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv, g
+
+    # MoE: 4096 tokens x top-8 of 256 experts (Zipf), w1|w3 [4096, 7168], w2 [7168, 2048] per expert
+    T, E, K8, D, I = 4096, syn.MOE_EXPERTS, syn.MOE_TOPK, syn.MOE_DIM, syn.MOE_INTER
+    rt = syn.moe_routing(T=T, E=E, topk=K8)
+    w13q = torch.empty((E, 2 * I, D), dtype=torch.float8_e4m3fn, device=dev)
+    w13s = torch.empty((E, 2 * I // 128, D // 128), dtype=torch.float32, device=dev)
+    w2q = torch.empty((E, D, I), dtype=torch.float8_e4m3fn, device=dev)
+    w2s = torch.empty((E, D // 128, I // 128), dtype=torch.float32, device=dev)
+    for e in range(E):
+        wcat = torch.cat([syn.moe_expert_weight_device(e, "w1"), syn.moe_expert_weight_device(e, "w3")], 0)
+        fp8.fp8_weight_quant(wcat, q=w13q[e], s=w13s[e])
+        fp8.fp8_weight_quant(syn.moe_expert_weight_device(e, "w2"), q=w2q[e], s=w2s[e])
+    del wcat
+    x = syn.normal_bf16_device((T, D), 1.0, 5, dev)
+    ids = torch.from_numpy(rt.ids).cuda()
+    wts = torch.from_numpy(rt.weights).cuda()
+    R = T * K8
+    xq = torch.empty((T, D), dtype=torch.float8_e4m3fn, device=dev)
+    xs = torch.empty((T, D // 128), dtype=torch.float32, device=dev)
+    st = {}
+
+    def moe():
+        off, pr, rtok = fp8.fp8_moe_route(ids, E)
+        fp8.fp8_act_quant(x, y=xq, s=xs)
+        aq, as_ = fp8.fp8_moe_gather(xq, xs, rtok)
+        if ext:
+            ev[0].record()
+        h, _ = fp8.fp8_grouped_gemm(aq, as_, w13q, w13s, off)
+        if ext:
+            ev[1].record()
+        gq_, gs_, _ = fp8.fp8_silu_mul_quant(h, h[:, I:], 2 * I, R, I)
+        if ext:
+            ev[2].record()
+        o2, _ = fp8.fp8_grouped_gemm(gq_, gs_, w2q, w2s, off)
+        if ext:
+            ev[3].record()
+        st["y"] = fp8.fp8_moe_combine(o2, wts, pr)[0]
+    g = capture(torch, moe)
+    ms = time_graph(torch, g, 5)
+    flops = R * (gemm_flops(1, 2 * I, D) + gemm_flops(1, D, I))
+    wbytes = E * (2 * I * D + D * I)
+    row = {"workload": "MoE 4096 tok x top-8 of 256, 7168->2x2048->7168", "ms": ms,
+           "TFLOP/s": flops / ms / 1e9, "weight_GB/s": wbytes / ms / 1e6,
+           "roofline_ms": max(wbytes / hbm / 1e6, flops / fp8_peak / 1e9)}
+    if ext:
+        g.replay()
+        torch.cuda.synchronize()
+        row["grouped_w13_ms"] = ev[0].elapsed_time(ev[1])
+        row["grouped_w2_ms"] = ev[2].elapsed_time(ev[3])
+    out["moe"] = row
+    del w13q, w2q, g
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    oracle.lib()
+    # same workload as our arm, on the host: bf16 weights and activations drawn
+    # once on the host, each step a bounded sample (1/16 of the output features)
+    frac = 16
+    dec_inputs = []
+    rs = np.random.default_rng(syn.SEED_BASE + 1)
+    for name in LAYERS:
+        N, K = syn.DECODE_LAYERS[name]
+        n_s = max(128, (N // frac) // 128 * 128)
+        w = syn.normal_bf16(rs, (n_s, K), 0.02)
+        wq, ws = oracle.weight_quant(w)
+        x = syn.normal_bf16(rs, (M_DECODE, K), 1.0, 0.005, 30.0)
+        dec_inputs.append((x, wq, ws, n_s, K))
+
+    def one():
+        nb = 0
+        for x, wq, ws, n_s, K in dec_inputs:
+            aq, as_ = oracle.act_quant(x)
+            oracle.gemm(aq, as_, wq, ws)
+            nb += act_quant_bytes(M_DECODE, K) + gemm_bytes(M_DECODE, n_s, K)
+        return nb
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += one()
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": "block-scaled FP8 linear HBM GB/s (decode-shaped linears)",
+            "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode linears wq_a/wq_b/wo, M=16 tokens, e4m3 weights 128x128 fp32 scales",
+                       "global_batch": M_DECODE, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": omp_threads(), "kind": "oracle",
+                             "sample": f"per step: act_quant of all 3 inputs + GEMM over 1/{frac} of each "
+                                       f"layer's output features (bytes scaled to the sample)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    import fp8_block_scaled_07_gb300 as fp8
+    peaks, peak_src = load_peaks()
+    dec = Decode(fp8, torch)
+    M = dec.M
+
+    # graphs: one per weight rotation, with external timing events around each GEMM
+    events = [[[make_event(torch, True), make_event(torch, True)] for _ in LAYERS] for _ in range(dec.R)]
+    have_ev = all(e is not None for r in events for l in r for e in l)
+    graphs = [capture(torch, lambda r=r: dec.step(r, events=events[r] if have_ev else None))
+              for r in range(dec.R)]
+    for i in range(args.warmup):
+        graphs[i % dec.R].replay()
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk.mark("t0")
+    t_start.record()
+    for i in range(args.steps):
+        graphs[i % dec.R].replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    clk.mark("t1")
+    if pg:
+        pg.barrier()
+    clocks = clk.stop()
+    ms = t_start.elapsed_time(t_end)
+    fp8.fp8_device_status()
+
+    # per-launch GEMM durations from the last replay of every rotation graph
+    gemm_ms, gemm_b = 0.0, 0
+    per_layer = {}
+    if have_ev:
+        for r in range(dec.R):
+            for i, name in enumerate(LAYERS):
+                t = events[r][i][0].elapsed_time(events[r][i][1])
+                gemm_ms += t
+                N, K = syn.DECODE_LAYERS[name]
+                gemm_b += gemm_bytes(M, N, K)
+                per_layer.setdefault(name, []).append(t)
+
+    ms_max = ms
+    if pg:
+        t = torch.tensor([ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max = float(t.item())
+    step_bytes = decode_step_bytes(M)
+    step_flops = decode_step_flops(M)
+    ms_per_step = ms_max / args.steps
+    value = world * step_bytes / (ms_per_step * 1e6)          # GB/s, all ranks
+
+    # e2e through the binding with host buffers
+    x_host = {n: dec.x[0][n].cpu().pin_memory() for n in LAYERS}
+    y_host = {n: torch.empty(dec.y[n].shape, dtype=torch.bfloat16).pin_memory() for n in LAYERS}
+    x_dev = {n: torch.empty_like(dec.x[0][n]) for n in LAYERS}
+    h2d = sum(x_host[n].numel() * 2 for n in LAYERS)
+    d2h = sum(y_host[n].numel() * 2 for n in LAYERS)
+
+    def e2e_step(r):
+        for n in LAYERS:
+            x_dev[n].copy_(x_host[n], non_blocking=True)
+        dec.step(r, x=x_dev)
+        for n in LAYERS:
+            y_host[n].copy_(dec.y[n], non_blocking=True)
+    for i in range(5):
+        e2e_step(i % dec.R)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        e2e_step(i % dec.R)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if pg:
+        t = torch.tensor([e2e_s], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * step_bytes * args.e2e_steps / e2e_s / 1e9
+
+    line = {
+        "metric": "block-scaled FP8 linear HBM GB/s (decode-shaped linears)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out", "data": "synthetic",
+        "config": {"workload": "decode linears wq_a 7168->1536, wq_b 1536->24576, wo 16384->7168; "
+                               "M=16 tokens; act_quant + fp8_gemm per layer",
+                   "global_batch": M * world, "parallelism": f"replicas x{world}",
+                   "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
+                   "launch": "CUDA graph per step"},
+        "tflops": world * step_flops / (ms_per_step * 1e9),
+        "gpu_launches": 6 * args.steps,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s / args.e2e_steps * 1e3, "path": "python binding, pinned host buffers, no graph"},
+        "clocks": clocks,
+        "peaks_source": peak_src,
+    }
+    if have_ev and gemm_ms > 0:
+        achieved = gemm_b / gemm_ms / 1e6
+        line["roofline"] = {"kernel": "fp8_gemm (swap-AB, stream-K)", "bound": "hbm", "achieved": achieved,
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                            "peak_kind": f"{peak_src} copy bandwidth",
+                            "traffic": profiled_traffic("fp8_gemm", "decode_M16"),
+                            "launch_us": {n: float(np.mean(v)) * 1e3 for n, v in per_layer.items()}}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        secs, nb, fl = oracle_decode_sample(torch, dec, 16)
+        line["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": omp_threads(), "kind": "oracle",
+                                "sample": "one decode step: act_quant of all 3 inputs + GEMM over 1/16 of each "
+                                          "layer's output features", "seconds": secs}
+    if rank == 0 and world == 1 and not args.no_rows:
+        del graphs
+        line["rows"] = rows_measurements(fp8, torch, peaks)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,290 @@
+"""GB300 (sm_103a) FP8 block-scaled linear: thin Python binding of the C ABI.
+
+Every function here marshals torch tensors into the C entry point of the
+same name declared in ``include/fp8bs.h`` and launches on the current CUDA
+stream; all arithmetic runs in the library's kernels.  There is no CPU
+fallback: importing this package fails if the shared library was not built
+(``python fp8_block_scaled_07_gb300/_build.py`` or
+``__graft_entry__.build()``), and every call raises :class:`Fp8Error` when
+the library returns a non-OK status.
+
+Tensors: bf16 as ``torch.bfloat16``; e4m3 as ``torch.float8_e4m3fn`` (a
+``torch.uint8`` view of the same bytes is accepted); scales ``torch.float32``.
+Outputs are allocated with torch (the caller's allocator) unless given.
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfp8bs.so")
+
+FP8_SCALE_FP32 = 0
+FP8_SCALE_UE8M0 = 1
+BLOCK = 128
+
+_STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID_ARG", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_ERR_CUDA",
+           4: "FP8_ERR_TIMEOUT", 5: "FP8_ERR_WORKSPACE"}
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn}: {_STATUS.get(status, status)} ({msg})")
+        self.status = status
+
+
+def _declare(lib):
+    vp, i64, i32, f32p, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+    st = ctypes.c_int
+    sigs = {
+        "fp8_act_quant": (st, [vp, vp, f32p, i64, i64, ctypes.c_int, vp]),
+        "fp8_weight_quant": (st, [vp, vp, f32p, i64, i64, ctypes.c_int, vp]),
+        "fp8_weight_dequant": (st, [vp, f32p, vp, i64, i64, vp]),
+        "fp8_gemm_workspace_size": (sz, [i64, i64, i64]),
+        "fp8_gemm": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, vp, sz, vp]),
+        "fp8_grouped_gemm": (st, [vp, f32p, vp, f32p, vp, i32, i64, vp, f32p, i64, i64, vp]),
+        "fp8_silu_mul_quant": (st, [vp, vp, i64, i64, i64, vp, f32p, vp, ctypes.c_int, vp]),
+        "fp8_moe_route": (st, [vp, i64, i32, i32, vp, vp, vp, vp]),
+        "fp8_moe_gather": (st, [vp, f32p, vp, i64, i64, vp, f32p, vp]),
+        "fp8_moe_combine": (st, [vp, f32p, vp, i64, i32, i64, vp, f32p, vp]),
+        "fp8_device_status": (st, [vp]),
+        "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "fp8_num_sms": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "fp8_block_scaled_07_gb300: native library %s is missing; build it with "
+            "`python fp8_block_scaled_07_gb300/_build.py` (there is no CPU fallback)" % LIB_PATH)
+    return _declare(ctypes.CDLL(LIB_PATH))
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------------ helpers
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name, status):
+    if status != 0:
+        raise Fp8Error(name, status, lib.fp8_status_string(status).decode())
+
+
+def _cuda(t, name, dtypes, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+_E4M3 = (torch.float8_e4m3fn, torch.uint8)
+_BF16 = (torch.bfloat16,)
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+
+
+def _empty_e4m3(shape, device):
+    return torch.empty(shape, dtype=torch.float8_e4m3fn, device=device)
+
+
+# ------------------------------------------------------------------ ops
+def fp8_act_quant(x, scale_fmt=FP8_SCALE_FP32, y=None, s=None, stream=None):
+    """x [M, K] bf16 -> (y [M, K] e4m3, s [M, K/128] fp32)."""
+    _cuda(x, "x", _BF16, 2)
+    M, K = x.shape
+    y = _empty_e4m3((M, K), x.device) if y is None else _cuda(y, "y", _E4M3)
+    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=x.device) if s is None else _cuda(s, "s", _F32)
+    _check("fp8_act_quant", lib.fp8_act_quant(_ptr(x), _ptr(y), _ptr(s), M, K, int(scale_fmt), _stream(stream)))
+    return y, s
+
+
+def fp8_weight_quant(w, scale_fmt=FP8_SCALE_FP32, q=None, s=None, stream=None):
+    """w [N, K] bf16 -> (q [N, K] e4m3, s [ceil(N/128), ceil(K/128)] fp32)."""
+    _cuda(w, "w", _BF16, 2)
+    N, K = w.shape
+    q = _empty_e4m3((N, K), w.device) if q is None else _cuda(q, "q", _E4M3)
+    if s is None:
+        s = torch.empty(((N + BLOCK - 1) // BLOCK, (K + BLOCK - 1) // BLOCK), dtype=torch.float32, device=w.device)
+    _check("fp8_weight_quant", lib.fp8_weight_quant(_ptr(w), _ptr(q), _ptr(s), N, K, int(scale_fmt), _stream(stream)))
+    return q, s
+
+
+def fp8_weight_dequant(w, s, y=None, stream=None):
+    """w [M, N] e4m3, s [ceil(M/128), ceil(N/128)] -> y [M, N] bf16."""
+    _cuda(w, "w", _E4M3, 2)
+    _cuda(s, "s", _F32, 2)
+    M, N = w.shape
+    if tuple(s.shape) != ((M + BLOCK - 1) // BLOCK, (N + BLOCK - 1) // BLOCK):
+        raise ValueError("scale grid shape mismatch")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=w.device) if y is None else _cuda(y, "y", _BF16)
+    _check("fp8_weight_dequant", lib.fp8_weight_dequant(_ptr(w), _ptr(s), _ptr(y), M, N, _stream(stream)))
+    return y
+
+
+class _Workspace:
+    """Zero-filled per-(device, stream) workspace, grown on demand.  The
+    library leaves it zero-filled after every successful call."""
+
+    def __init__(self):
+        self._bufs = {}
+        self._lock = threading.Lock()
+
+    def get(self, nbytes, device, stream):
+        if nbytes == 0:
+            return None
+        key = (device.index, stream.cuda_stream)
+        with self._lock:
+            buf = self._bufs.get(key)
+            if buf is None or buf.numel() < nbytes:
+                buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+                self._bufs[key] = buf
+            return buf
+
+    def reset(self):
+        with self._lock:
+            for b in self._bufs.values():
+                b.zero_()
+
+
+workspaces = _Workspace()
+
+
+def fp8_gemm_workspace_size(M, N, K):
+    return int(lib.fp8_gemm_workspace_size(M, N, K))
+
+
+def fp8_gemm(a, a_s, b, b_s, out_bf16=True, out_fp32=False, c_bf16=None, c_fp32=None,
+             workspace=None, stream=None):
+    """C = fp8 block-scaled a @ b^T.  Returns (c_bf16 or None, c_fp32 or None)."""
+    _cuda(a, "a", _E4M3, 2)
+    _cuda(b, "b", _E4M3, 2)
+    _cuda(a_s, "a_s", _F32, 2)
+    _cuda(b_s, "b_s", _F32, 2)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("K mismatch")
+    if tuple(a_s.shape) != (M, K // BLOCK) or tuple(b_s.shape) != ((N + BLOCK - 1) // BLOCK, K // BLOCK):
+        raise ValueError("scale shape mismatch")
+    if c_bf16 is None and out_bf16:
+        c_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if c_fp32 is None and out_fp32:
+        c_fp32 = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    st = torch.cuda.current_stream() if stream is None else stream
+    if workspace is None:
+        workspace = workspaces.get(fp8_gemm_workspace_size(M, N, K), a.device, st)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("fp8_gemm", lib.fp8_gemm(_ptr(a), _ptr(a_s), _ptr(b), _ptr(b_s), _ptr(c_bf16), _ptr(c_fp32),
+                                    M, N, K, _ptr(workspace), ws_bytes, _stream(st)))
+    return c_bf16, c_fp32
+
+
+def fp8_grouped_gemm(a, a_s, b, b_s, offsets, out_bf16=True, out_fp32=False, c_bf16=None,
+                     c_fp32=None, stream=None):
+    """Per-expert fp8 GEMM over packed rows; offsets int32 [G+1] on the device."""
+    _cuda(a, "a", _E4M3, 2)
+    _cuda(b, "b", _E4M3, 3)
+    _cuda(a_s, "a_s", _F32, 2)
+    _cuda(b_s, "b_s", _F32, 3)
+    _cuda(offsets, "offsets", _I32, 1)
+    R, K = a.shape
+    G, N, Kb = b.shape
+    if Kb != K or offsets.numel() != G + 1:
+        raise ValueError("shape mismatch")
+    if c_bf16 is None and out_bf16:
+        c_bf16 = torch.empty((R, N), dtype=torch.bfloat16, device=a.device)
+    if c_fp32 is None and out_fp32:
+        c_fp32 = torch.empty((R, N), dtype=torch.float32, device=a.device)
+    _check("fp8_grouped_gemm", lib.fp8_grouped_gemm(_ptr(a), _ptr(a_s), _ptr(b), _ptr(b_s), _ptr(offsets),
+                                                    G, R, _ptr(c_bf16), _ptr(c_fp32), N, K, _stream(stream)))
+    return c_bf16, c_fp32
+
+
+def fp8_silu_mul_quant(h1, h3, ld_h, R, I, scale_fmt=FP8_SCALE_FP32, want_g=False, y=None, s=None,
+                       stream=None):
+    """g = bf16(bf16(silu(h1)) * h3) then act_quant(g).  h1/h3 are views into
+    bf16 storage with row stride ld_h.  Returns (y, s, g or None)."""
+    for name, t in (("h1", h1), ("h3", h3)):
+        if not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    dev = h1.device
+    y = _empty_e4m3((R, I), dev) if y is None else y
+    s = torch.empty((R, I // BLOCK), dtype=torch.float32, device=dev) if s is None else s
+    g = torch.empty((R, I), dtype=torch.bfloat16, device=dev) if want_g else None
+    _check("fp8_silu_mul_quant", lib.fp8_silu_mul_quant(_ptr(h1), _ptr(h3), ld_h, R, I, _ptr(y), _ptr(s),
+                                                        _ptr(g), int(scale_fmt), _stream(stream)))
+    return y, s, g
+
+
+def fp8_moe_route(ids, n_experts, stream=None):
+    """ids int32 [T, topk] -> (offsets [E+1], pair_row [T, topk], row_token [T*topk])."""
+    _cuda(ids, "ids", _I32, 2)
+    T, topk = ids.shape
+    offsets = torch.empty(n_experts + 1, dtype=torch.int32, device=ids.device)
+    pair_row = torch.empty((T, topk), dtype=torch.int32, device=ids.device)
+    row_token = torch.empty(T * topk, dtype=torch.int32, device=ids.device)
+    _check("fp8_moe_route", lib.fp8_moe_route(_ptr(ids), T, topk, n_experts, _ptr(offsets), _ptr(pair_row),
+                                              _ptr(row_token), _stream(stream)))
+    return offsets, pair_row, row_token
+
+
+def fp8_moe_gather(xq, xs, row_token, aq=None, as_=None, stream=None):
+    _cuda(xq, "xq", _E4M3, 2)
+    _cuda(xs, "xs", _F32, 2)
+    _cuda(row_token, "row_token", _I32, 1)
+    R = row_token.numel()
+    K = xq.shape[1]
+    aq = _empty_e4m3((R, K), xq.device) if aq is None else aq
+    as_ = torch.empty((R, K // BLOCK), dtype=torch.float32, device=xq.device) if as_ is None else as_
+    _check("fp8_moe_gather", lib.fp8_moe_gather(_ptr(xq), _ptr(xs), _ptr(row_token), R, K, _ptr(aq), _ptr(as_),
+                                                _stream(stream)))
+    return aq, as_
+
+
+def fp8_moe_combine(out, w, pair_row, out_bf16=True, out_fp32=False, stream=None):
+    _cuda(out, "out", _BF16, 2)
+    _cuda(w, "w", _F32, 2)
+    _cuda(pair_row, "pair_row", _I32, 2)
+    T, topk = w.shape
+    D = out.shape[1]
+    yb = torch.empty((T, D), dtype=torch.bfloat16, device=out.device) if out_bf16 else None
+    yf = torch.empty((T, D), dtype=torch.float32, device=out.device) if out_fp32 else None
+    _check("fp8_moe_combine", lib.fp8_moe_combine(_ptr(out), _ptr(w), _ptr(pair_row), T, topk, D, _ptr(yb),
+                                                  _ptr(yf), _stream(stream)))
+    return yb, yf
+
+
+def fp8_device_status(stream=None):
+    """Synchronise and return the library's device status (raises on error)."""
+    _check("fp8_device_status", lib.fp8_device_status(_stream(stream)))
+
+
+def fp8_num_sms():
+    return int(lib.fp8_num_sms())
+
+
+def fp8_linear(x, w, w_s, scale_fmt=FP8_SCALE_FP32, out_fp32=False, stream=None):
+    """The FP8 branch of the model's linear(): act_quant(x) then fp8_gemm."""
+    xq, xs = fp8_act_quant(x, scale_fmt, stream=stream)
+    return fp8_gemm(xq, xs, w, w_s, out_bf16=True, out_fp32=out_fp32, stream=stream)

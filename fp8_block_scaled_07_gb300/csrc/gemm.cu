@@ -1,0 +1,681 @@
+// gemm.cu -- block-scaled FP8 GEMM on sm_103a tensor cores.
+//
+// What it computes ("Data flow -- deepseek-ai/DeepSeek-V3", bullet "FP8
+// quantization data flow"; source tour "DeepSeek-V3", paragraph "FP8 with
+// per-block scales"):
+//   C[m, n] = sum_kb a_s[m, kb] * b_s[n/128, kb] * sum_{k in kb} a[m,k] b[n,k]
+// with e4m3 operands, fp32 scales and fp32 accumulation; the grouped form
+// runs the same product per routed expert over packed rows ("Behavior
+// traces", bullet "MoE trace"; source tour, "Honest Limits").
+//
+// How (GB300-native, not the pages' Triton design):
+//   * one 128-K slab is one pipeline stage: TMA brings a 128x128 e4m3 tile
+//     of the "P" operand and a BNx128 tile of the "Q" operand into shared
+//     memory (128-byte swizzle); one thread issues four K=32
+//     tcgen05.mma.kind::f8f6f4 into a fresh TMEM slab buffer (128 lanes x
+//     BN fp32 columns);
+//   * four epilogue warps read the finished slab from TMEM (tcgen05.ld),
+//     multiply by the slab's scale product a_s*b_s and accumulate in fp32
+//     registers ("promotion"), while the tensor core fills the other slab
+//     buffer;
+//   * warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
+//     owner), warps 4..7 = epilogue; persistent CTAs, one per SM;
+//   * decode shapes (M <= 64) swap the operands: the weight fills the
+//     128-row MMA side and the tokens the N side (16..64);
+//   * few tiles -> stream-K: each CTA takes an equal run of (tile, slab)
+//     units; tiles split across CTAs are reduced deterministically by the
+//     CTA that finishes a tile last (fp32 partials in the caller's
+//     workspace, one atomic ticket per tile, no spinning).
+// Every mbarrier wait is bounded (see common.cuh).
+#include "common.cuh"
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace fp8bs {
+
+__device__ int g_gemm_status;   // FP8_OK or FP8_ERR_TIMEOUT, read by fp8_device_status
+
+namespace {
+
+constexpr int kNumThreads = 256;
+constexpr int kEpiWarp0 = 4;               // epilogue warps 4..7 (warp % 4 = TMEM lane quarter)
+constexpr int kPTileBytes = 128 * kBlock;  // 128 rows x 128 e4m3
+constexpr int kMaxGroups = 1024;
+// Workspace layout: a fixed block of stream-K tile counters (which must stay
+// zero between calls, whatever shape used the workspace before), then the
+// fp32 partial tiles (no requirement on their contents).
+constexpr int kMaxSkTiles = 4096;
+constexpr size_t kCounterBytes = kMaxSkTiles * sizeof(int);
+
+enum Variant { kDense = 0, kDenseSwap = 1, kGrouped = 2 };
+
+struct Params {
+    const float* a_s;          // [rows_a, KB]
+    const float* b_s;          // [G][NB][KB]
+    const int32_t* offsets;    // grouped: [G+1] (device)
+    __nv_bfloat16* c_bf16;     // [rows, N] or null
+    float* c_fp32;             // [rows, N] or null
+    float* partials;           // stream-K workspace
+    int* counters;             // stream-K tickets, one per tile
+    int M;                     // rows of A (grouped: rows covered by offsets <= R_max)
+    int N;                     // columns of C (per expert when grouped)
+    int KB;                    // K / 128
+    int NB;                    // ceil(N / 128)
+    int G;                     // experts (grouped)
+    int tiles_p, tiles_q;      // dense tile grid (P rows / 128, Q rows / BN)
+    int num_tiles;             // dense
+    int stream_k;              // 1: stream-K schedule over total_units
+    long long total_units;     // num_tiles * KB
+};
+
+struct Tile {
+    int p_row0, q_row0;   // TMA row coordinates of the P and Q tiles
+    int p_valid, q_valid; // rows of the tile that hold real data
+    int group;            // expert (grouped) else 0
+    int q_col0;           // grouped: first output column of the tile
+};
+
+struct Seg {
+    int tile, k0, k1;
+};
+
+template <int BN>
+struct Cfg {
+    static constexpr int kQTileBytes = BN * kBlock;
+    static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
+    static constexpr int kStages = BN >= 128 ? 6 : 8;
+    static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,32,64,128}
+    static constexpr int kBarBytes = 1024;
+    static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes +
+                                      (kMaxGroups + 1) * 4;
+};
+
+// ------------------------------------------------------------------ schedule
+__device__ __forceinline__ long long sk_start(long long c, long long U, long long P) {
+    return c * U / P;
+}
+__device__ __forceinline__ int sk_owner(long long u, long long U, int P) {
+    long long c = u * P / U;
+    while (c + 1 < P && sk_start(c + 1, U, P) <= u) ++c;
+    while (c > 0 && sk_start(c, U, P) > u) --c;
+    return static_cast<int>(c);
+}
+
+struct SegIter {
+    // data-parallel: tiles blockIdx.x + i * gridDim.x; stream-K: units [lo, hi)
+    long long u, hi;
+    int t, stride, num_tiles, KB;
+    bool sk;
+    __device__ void init(const Params& p, int ntiles) {
+        KB = p.KB;
+        sk = p.stream_k != 0;
+        num_tiles = ntiles;
+        if (sk) {
+            u = sk_start(blockIdx.x, p.total_units, gridDim.x);
+            hi = sk_start(blockIdx.x + 1, p.total_units, gridDim.x);
+        } else {
+            t = blockIdx.x;
+            stride = gridDim.x;
+        }
+    }
+    __device__ bool next(Seg& s) {
+        if (sk) {
+            if (u >= hi) return false;
+            s.tile = static_cast<int>(u / KB);
+            s.k0 = static_cast<int>(u - static_cast<long long>(s.tile) * KB);
+            long long end = static_cast<long long>(s.tile + 1) * KB;
+            if (end > hi) end = hi;
+            s.k1 = static_cast<int>(end - static_cast<long long>(s.tile) * KB);
+            u = end;
+            return true;
+        }
+        if (t >= num_tiles) return false;
+        s.tile = t;
+        s.k0 = 0;
+        s.k1 = KB;
+        t += stride;
+        return true;
+    }
+};
+
+// Grouped: per-expert m-tiles (ceil(rows/128)) x N/BN n-tiles; tile index
+// runs m-fastest inside an expert so CTAs working at the same time share the
+// expert's weight tile through L2.
+template <int BN, int V>
+__device__ __forceinline__ Tile tile_geom(const Params& p, int t, const int* s_prefix) {
+    Tile g{};
+    if (V == kDense) {
+        const int tp = t % p.tiles_p, tq = t / p.tiles_p;
+        g.p_row0 = tp * 128;
+        g.q_row0 = tq * BN;
+        g.p_valid = min(128, p.M - g.p_row0);
+        g.q_valid = min(BN, p.N - g.q_row0);
+    } else if (V == kDenseSwap) {
+        const int tp = t % p.tiles_p, tq = t / p.tiles_p;
+        g.p_row0 = tp * 128;         // weight rows (output columns)
+        g.q_row0 = tq * BN;          // token rows
+        g.p_valid = min(128, p.N - g.p_row0);
+        g.q_valid = min(BN, p.M - g.q_row0);
+    } else {
+        int lo = 0, hi = p.G;        // largest g with s_prefix[g] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int grp = lo;
+        const int r0 = p.offsets[grp], cnt = p.offsets[grp + 1] - r0;
+        const int mt = (cnt + 127) / 128;
+        const int local = t - s_prefix[grp];
+        const int tp = local % mt, tq = local / mt;
+        g.group = grp;
+        g.p_row0 = r0 + tp * 128;
+        g.p_valid = min(128, cnt - tp * 128);
+        g.q_col0 = tq * BN;
+        g.q_row0 = grp * p.N + tq * BN;
+        g.q_valid = min(BN, p.N - tq * BN);
+    }
+    return g;
+}
+
+__device__ __forceinline__ void set_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_TIMEOUT));
+}
+
+// Store BN accumulators of one output row (non-swapped layout) or one
+// output column (swapped layout).
+template <int BN, int V>
+__device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int e,
+                                           const float (&acc)[BN]) {
+    if (V == kDenseSwap) {
+        const int n = tg.p_row0 + e;
+        if (e >= tg.p_valid) return;
+#pragma unroll
+        for (int j = 0; j < BN; ++j) {
+            if (j < tg.q_valid) {
+                const int64_t idx = static_cast<int64_t>(tg.q_row0 + j) * p.N + n;
+                if (p.c_bf16) p.c_bf16[idx] = __float2bfloat16_rn(acc[j]);
+                if (p.c_fp32) p.c_fp32[idx] = acc[j];
+            }
+        }
+        return;
+    }
+    if (e >= tg.p_valid) return;
+    const int64_t row = tg.p_row0 + e;
+    const int col0 = (V == kGrouped) ? tg.q_col0 : tg.q_row0;
+    const bool vec = (p.N % 8 == 0);
+#pragma unroll
+    for (int j0 = 0; j0 < BN; j0 += 8) {
+        const int col = col0 + j0;
+        if (vec && j0 + 8 <= tg.q_valid) {
+            if (p.c_bf16) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __nv_bfloat162 b = __floats2bfloat162_rn(acc[j0 + 2 * i], acc[j0 + 2 * i + 1]);
+                    w[i] = *reinterpret_cast<uint32_t*>(&b);
+                }
+                *reinterpret_cast<uint4*>(p.c_bf16 + row * p.N + col) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (p.c_fp32) {
+                float4* d = reinterpret_cast<float4*>(p.c_fp32 + row * p.N + col);
+                d[0] = make_float4(acc[j0], acc[j0 + 1], acc[j0 + 2], acc[j0 + 3]);
+                d[1] = make_float4(acc[j0 + 4], acc[j0 + 5], acc[j0 + 6], acc[j0 + 7]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (j0 + i < tg.q_valid) {
+                    if (p.c_bf16) p.c_bf16[row * p.N + col + i] = __float2bfloat16_rn(acc[j0 + i]);
+                    if (p.c_fp32) p.c_fp32[row * p.N + col + i] = acc[j0 + i];
+                }
+            }
+        }
+    }
+}
+
+template <int BN, int V>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
+                const Params p) {
+    using C = Cfg<BN>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sP = smem;                                   // S x 16 KB
+    uint8_t* sQ = smem + S * kPTileBytes;                 // S x BN*128
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    uint64_t* full = bars;                 // S
+    uint64_t* empty = bars + S;            // S
+    uint64_t* tfull = bars + 2 * S;        // 2
+    uint64_t* tempty = bars + 2 * S + 2;   // 2
+    uint64_t* mma_done = bars + 2 * S + 4; // 1
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
+    int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kBarBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_p);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, C::kTmemCols);
+        tmem_relinquish();
+    }
+    int num_tiles = p.num_tiles;
+    if (V == kGrouped) {
+        // exclusive prefix over experts of (m-tiles x n-tiles)
+        const int tq = p.N / BN;
+        if (threadIdx.x == 0) {
+            int acc = 0;
+            for (int g = 0; g < p.G; ++g) {
+                s_prefix[g] = acc;
+                const int cnt = p.offsets[g + 1] - p.offsets[g];
+                acc += ((cnt + 127) / 128) * tq;
+            }
+            s_prefix[p.G] = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (V == kGrouped) num_tiles = s_prefix[p.G];
+    const uint32_t tmem_base = *tmem_holder;
+
+    SegIter it;
+    it.init(p, num_tiles);
+    Seg sg;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t iter = 0;
+            bool ok = true;
+            while (ok && it.next(sg)) {
+                const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
+                for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
+                    const int st = iter % S;
+                    if (!mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag)) {
+                        set_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                    tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
+                    tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
+                }
+            }
+            // drain: every load issued must land before the CTA may exit
+            for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
+                const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
+                const volatile int never = 0;
+                if (!mbar_wait(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
+            uint32_t iter = 0, slab = 0;
+            bool ok = true;
+            while (ok && it.next(sg)) {
+                for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter, ++slab) {
+                    const int st = iter % S;
+                    const int buf = slab & 1;
+                    if (!mbar_wait(&tempty[buf], ((slab >> 1) & 1) ^ 1, abort_flag) ||
+                        !mbar_wait(&full[st], (iter / S) & 1, abort_flag)) {
+                        set_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+                    const uint64_t da = smem_desc_sw128(smem_u32(sP + st * kPTileBytes));
+                    const uint64_t db = smem_desc_sw128(smem_u32(sQ + st * C::kQTileBytes));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)   // 4 x K=32 = one 128-K slab; +32 bytes each
+                        mma_e4m3(d, da + 2 * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+                    mma_commit(&empty[st]);
+                    mma_commit(&tfull[buf]);
+                }
+            }
+            mma_commit(mma_done);
+            const volatile int never = 0;
+            if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;                     // TMEM lane quarter
+        const int e = q * 32 + lane;                // row of the tile (TMEM lane)
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        uint32_t slab = 0;
+        bool ok = true;
+        while (ok && it.next(sg)) {
+            const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
+            float acc[BN];
+#pragma unroll
+            for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
+            // scale pointers
+            const float* ps;   // per-row (non-swap) / per-block (swap) scale of the P side
+            const float* qs;   // per-block (non-swap) / per-token (swap) scale of the Q side
+            if (V == kDenseSwap) {
+                ps = p.b_s + static_cast<int64_t>(tg.p_row0 / 128) * p.KB;
+                qs = p.a_s + static_cast<int64_t>(tg.q_row0) * p.KB;
+            } else if (V == kDense) {
+                ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
+                qs = p.b_s + static_cast<int64_t>(tg.q_row0 / 128) * p.KB;
+            } else {
+                ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
+                qs = p.b_s + (static_cast<int64_t>(tg.group) * p.NB + tg.q_col0 / 128) * p.KB;
+            }
+            for (int kb = sg.k0; kb < sg.k1; ++kb, ++slab) {
+                const int buf = slab & 1;
+                // scales of this slab (loaded before the wait to hide latency)
+                float sc[V == kDenseSwap ? BN : 1];
+                if constexpr (V == kDenseSwap) {
+                    const float sp = __ldg(ps + kb);
+#pragma unroll
+                    for (int j = 0; j < BN; ++j)
+                        sc[j] = j < tg.q_valid ? sp * __ldg(qs + static_cast<int64_t>(j) * p.KB + kb) : 0.0f;
+                } else {
+                    sc[0] = __ldg(ps + kb) * __ldg(qs + kb);
+                }
+                if (!mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag)) {
+                    set_abort(abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
+                if constexpr (BN == 16) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        acc[j] = fmaf(__uint_as_float(r[j]), sc[V == kDenseSwap ? j : 0], acc[j]);
+                } else {
+#pragma unroll
+                    for (int c0 = 0; c0 < BN; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(taddr + c0, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[c0 + j] = fmaf(__uint_as_float(r[j]),
+                                               sc[V == kDenseSwap ? c0 + j : 0], acc[c0 + j]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[buf]);
+            }
+            if (!ok) break;
+            if (sg.k0 == 0 && sg.k1 == p.KB) {
+                store_tile<BN, V>(p, tg, e, acc);
+                continue;
+            }
+            // ---- stream-K fixup (dense only): partial tile
+            const long long U = p.total_units;
+            const int P = gridDim.x;
+            const long long u_first = static_cast<long long>(sg.tile) * p.KB;
+            const int c_first = sk_owner(u_first, U, P);
+            const int c_last = sk_owner(u_first + p.KB - 1, U, P);
+            const int nseg = c_last - c_first + 1;
+            auto slot_of = [&](int c) -> float* {
+                const int first_tile = static_cast<int>(sk_start(c, U, P) / p.KB);
+                const int which = (first_tile == sg.tile) ? 0 : 1;
+                return p.partials + (static_cast<int64_t>(c) * 2 + which) * (128 * BN);
+            };
+            float* mine = slot_of(blockIdx.x);
+#pragma unroll
+            for (int j = 0; j < BN; ++j) __stcg(mine + j * 128 + e, acc[j]);
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (e == 0) *ticket_box = atomicAdd(p.counters + sg.tile, 1);
+            named_bar_sync(1, 128);
+            const int ticket = *ticket_box;
+            named_bar_sync(1, 128);
+            if (ticket == nseg - 1) {
+                __threadfence();
+#pragma unroll
+                for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
+                for (int si = 0; si < nseg; ++si) {
+                    const float* src = slot_of(c_first + si);
+#pragma unroll
+                    for (int j = 0; j < BN; ++j) acc[j] += __ldcg(src + j * 128 + e);
+                }
+                store_tile<BN, V>(p, tg, e, acc);
+                if (e == 0) p.counters[sg.tile] = 0;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over an e4m3 matrix [rows, K] (row stride K bytes), box 128 x box_rows.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlock), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int variant;   // kDense / kDenseSwap
+    int bn;
+    int tiles_p, tiles_q, num_tiles;
+    int stream_k;
+    int grid;
+    long long total_units;
+    size_t ws_bytes;   // counters + partial slots
+    size_t counters_bytes;
+};
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
+    Plan pl{};
+    const int KB = static_cast<int>(K / kBlock);
+    if (M <= 64) {
+        pl.variant = kDenseSwap;
+        pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+        pl.tiles_p = static_cast<int>((N + 127) / 128);
+        pl.tiles_q = static_cast<int>((M + pl.bn - 1) / pl.bn);
+    } else {
+        pl.variant = kDense;
+        pl.bn = 128;
+        pl.tiles_p = static_cast<int>((M + 127) / 128);
+        pl.tiles_q = static_cast<int>((N + 127) / 128);
+    }
+    pl.num_tiles = pl.tiles_p * pl.tiles_q;
+    pl.total_units = static_cast<long long>(pl.num_tiles) * KB;
+    if (pl.num_tiles >= 4 * sms || pl.num_tiles > kMaxSkTiles || KB == 1) {
+        pl.stream_k = 0;
+        pl.grid = std::min(pl.num_tiles, sms);
+        pl.ws_bytes = 0;
+    } else {
+        pl.stream_k = 1;
+        // at least 2 slabs per CTA so the pipeline has something to overlap
+        long long g = std::min<long long>(sms, std::max<long long>(1, pl.total_units / 2));
+        pl.grid = static_cast<int>(g);
+        pl.counters_bytes = kCounterBytes;
+        pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.grid) * 2 * 128 * pl.bn * 4;
+    }
+    return pl;
+}
+
+template <int BN, int V>
+cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& prm, int grid,
+                   cudaStream_t st) {
+    constexpr int smem = Cfg<BN>::kSmemBytes;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, V>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    gemm_kernel<BN, V><<<grid, kNumThreads, smem, st>>>(mp, mq, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_read_and_clear_status(cudaStream_t st) {
+    int v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_gemm_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_gemm_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return -1;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % kBlock != 0) return 0;
+    return make_plan(M, N, K, device_sm_count()).ws_bytes;
+}
+
+extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
+                               void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (M < 0 || N < 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    if (!a || !a_s || !b || !b_s || (!c_bf16 && !c_fp32)) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b)) return FP8_ERR_INVALID_ARG;
+    if ((c_bf16 && (reinterpret_cast<uintptr_t>(c_bf16) & 1)) ||
+        (c_fp32 && (reinterpret_cast<uintptr_t>(c_fp32) & 3)))
+        return FP8_ERR_INVALID_ARG;
+    if (N % 8 == 0 && ((c_bf16 && !aligned16(c_bf16)) || (c_fp32 && !aligned16(c_fp32))))
+        return FP8_ERR_INVALID_ARG;
+    const Plan pl = make_plan(M, N, K, device_sm_count());
+    if (pl.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pl.ws_bytes))
+        return FP8_ERR_WORKSPACE;
+
+    Params prm{};
+    prm.a_s = a_s;
+    prm.b_s = b_s;
+    prm.c_bf16 = static_cast<__nv_bfloat16*>(c_bf16);
+    prm.c_fp32 = c_fp32;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.KB = static_cast<int>(K / kBlock);
+    prm.NB = static_cast<int>((N + 127) / 128);
+    prm.G = 1;
+    prm.tiles_p = pl.tiles_p;
+    prm.tiles_q = pl.tiles_q;
+    prm.num_tiles = pl.num_tiles;
+    prm.stream_k = pl.stream_k;
+    prm.total_units = pl.total_units;
+    if (pl.ws_bytes > 0) {
+        prm.counters = static_cast<int*>(workspace);
+        prm.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
+    }
+    CUtensorMap mp, mq;
+    const bool swap = pl.variant == kDenseSwap;
+    // P: 128-row tiles; Q: BN-row tiles
+    if (!make_map(&mp, swap ? b : a, swap ? N : M, K, 128) ||
+        !make_map(&mq, swap ? a : b, swap ? M : N, K, pl.bn))
+        return FP8_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (!swap) {
+        e = launch<128, kDense>(mp, mq, prm, pl.grid, st);
+    } else if (pl.bn == 16) {
+        e = launch<16, kDenseSwap>(mp, mq, prm, pl.grid, st);
+    } else if (pl.bn == 32) {
+        e = launch<32, kDenseSwap>(mp, mq, prm, pl.grid, st);
+    } else {
+        e = launch<64, kDenseSwap>(mp, mq, prm, pl.grid, st);
+    }
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const void* b,
+                                       const float* b_s, const int32_t* offsets, int32_t G,
+                                       int64_t R_max, void* c_bf16, float* c_fp32, int64_t N,
+                                       int64_t K, void* stream) {
+    if (G < 0 || G > kMaxGroups || R_max < 0 || N < 0 || K <= 0 || K % kBlock != 0)
+        return FP8_ERR_INVALID_ARG;
+    if (G == 0 || R_max == 0 || N == 0) return FP8_OK;
+    if (N % 128 != 0) return FP8_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(G) * N > (1LL << 31) - 1 || R_max > (1LL << 31) - 1)
+        return FP8_ERR_UNSUPPORTED;
+    if (!a || !a_s || !b || !b_s || !offsets || (!c_bf16 && !c_fp32)) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || (c_bf16 && !aligned16(c_bf16)) ||
+        (c_fp32 && !aligned16(c_fp32)))
+        return FP8_ERR_INVALID_ARG;
+    Params prm{};
+    prm.a_s = a_s;
+    prm.b_s = b_s;
+    prm.offsets = offsets;
+    prm.c_bf16 = static_cast<__nv_bfloat16*>(c_bf16);
+    prm.c_fp32 = c_fp32;
+    prm.M = static_cast<int>(R_max);
+    prm.N = static_cast<int>(N);
+    prm.KB = static_cast<int>(K / kBlock);
+    prm.NB = static_cast<int>(N / 128);
+    prm.G = G;
+    prm.stream_k = 0;
+    CUtensorMap mp, mq;
+    if (!make_map(&mp, a, R_max, K, 128) || !make_map(&mq, b, static_cast<int64_t>(G) * N, K, 128))
+        return FP8_ERR_CUDA;
+    cudaError_t e = launch<128, kGrouped>(mp, mq, prm, device_sm_count(),
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}

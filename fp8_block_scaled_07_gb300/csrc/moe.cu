@@ -1,0 +1,179 @@
+// moe.cu -- data movement around the grouped expert GEMM
+// ("Behavior traces -- deepseek-ai/DeepSeek-V3", bullet "MoE trace": count
+// the tokens per expert, take each expert's tokens in order, run the expert
+// and add its output times the gate weight back into y).
+//
+//   route    stable counting sort of (token, slot) pairs by expert id; CTA e
+//            counts the pairs with id < e (its first packed row) and ranks
+//            the pairs with id == e by a block-wide ordered scan, so the
+//            result is deterministic and needs no atomics;
+//   gather   packed row r <- quantised token row row_token[r] (+ scales);
+//   combine  y[t] = sum_j w[t,j] * out[pair_row[t,j]] in fp32, one warp per
+//            token, 16-byte loads.
+#include "common.cuh"
+
+namespace fp8bs {
+namespace {
+
+constexpr int kRouteThreads = 256;
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t* __restrict__ ids,
+                                                              int64_t P, int32_t topk, int32_t E,
+                                                              int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ pair_row,
+                                                              int32_t* __restrict__ row_token) {
+    __shared__ int warp_cnt[kRouteThreads / 32];
+    __shared__ int warp_lt[kRouteThreads / 32];
+    __shared__ int s_base;
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // pass 1: number of pairs with id < e  -> first packed row of expert e
+    int lt = 0;
+    for (int64_t i = threadIdx.x; i < P; i += kRouteThreads) lt += (__ldg(ids + i) < e) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) lt += __shfl_xor_sync(0xFFFFFFFFu, lt, o);
+    if (lane == 0) warp_lt[warp] = lt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int w = 0; w < kRouteThreads / 32; ++w) s += warp_lt[w];
+        s_base = s;
+        offsets[e] = s;
+        if (e == E - 1) offsets[E] = static_cast<int32_t>(P);
+    }
+    __syncthreads();
+    int base = s_base;
+    // pass 2: ordered ranks of the pairs with id == e
+    for (int64_t c0 = 0; c0 < P; c0 += kRouteThreads) {
+        const int64_t i = c0 + threadIdx.x;
+        const bool hit = i < P && __ldg(ids + i) == e;
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, hit);
+        const int before_in_warp = __popc(ball & ((1u << lane) - 1u));
+        if (lane == 0) warp_cnt[warp] = __popc(ball);
+        __syncthreads();
+        int before = base + before_in_warp;
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kRouteThreads / 32; ++w) {
+            const int c = warp_cnt[w];
+            if (w < warp) before += c;
+            total += c;
+        }
+        if (hit) {
+            pair_row[i] = before;
+            row_token[before] = static_cast<int32_t>(i / topk);
+        }
+        base += total;
+        __syncthreads();
+    }
+}
+
+// One warp per packed row: K bytes of codes + K/128 scales.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ xq,
+                                                    const float* __restrict__ xs,
+                                                    const int32_t* __restrict__ row_token,
+                                                    int64_t R, int64_t K, uint4* __restrict__ aq,
+                                                    float* __restrict__ as) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t chunks = K / 16, KB = K / kBlock;
+    for (int64_t r = warp; r < R; r += nwarps) {
+        const int64_t t = __ldg(row_token + r);
+        const uint4* src = xq + t * chunks;
+        uint4* dst = aq + r * chunks;
+        for (int64_t c = lane; c < chunks; c += 32) dst[c] = __ldcs(src + c);
+        for (int64_t c = lane; c < KB; c += 32) as[r * KB + c] = __ldg(xs + t * KB + c);
+    }
+}
+
+// One warp per token; lane handles 8 consecutive columns per step.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ out,
+                                                     const float* __restrict__ w,
+                                                     const int32_t* __restrict__ pair_row,
+                                                     int64_t T, int32_t topk, int64_t D,
+                                                     uint4* __restrict__ y_bf16,
+                                                     float4* __restrict__ y_fp32) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t chunks = D / 8;
+    for (int64_t t = warp; t < T; t += nwarps) {
+        for (int64_t c = lane; c < chunks; c += 32) {
+            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int j = 0; j < topk; ++j) {
+                const int64_t r = __ldg(pair_row + t * topk + j);
+                const float wj = __ldg(w + t * topk + j);
+                const uint4 v = __ldcs(out + r * chunks + c);
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(wj, __uint_as_float(u[i] << 16), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wj, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                }
+            }
+            if (y_bf16) {
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+                    o[i] = *reinterpret_cast<uint32_t*>(&b);
+                }
+                y_bf16[t * chunks + c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (y_fp32) {
+                y_fp32[(t * chunks + c) * 2] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                y_fp32[(t * chunks + c) * 2 + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+        }
+    }
+}
+
+int warps_grid(int64_t warps_needed) {
+    int64_t g = (warps_needed + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    return static_cast<int>(g < 1 ? 1 : (g > cap ? cap : g));
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" fp8_status fp8_moe_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E,
+                                    int32_t* offsets, int32_t* pair_row, int32_t* row_token,
+                                    void* stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || E > 1024) return FP8_ERR_INVALID_ARG;
+    if (!offsets) return FP8_ERR_INVALID_ARG;
+    const int64_t P = T * topk;
+    if (P > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    if (P > 0 && (!ids || !pair_row || !row_token)) return FP8_ERR_INVALID_ARG;
+    route_kernel<<<E, kRouteThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        ids, P, topk, E, offsets, pair_row, row_token);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" fp8_status fp8_moe_gather(const void* xq, const float* xs, const int32_t* row_token,
+                                     int64_t R, int64_t K, void* aq, float* as, void* stream) {
+    if (R < 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
+    if (R == 0) return FP8_OK;
+    if (!xq || !xs || !row_token || !aq || !as || !aligned16(xq) || !aligned16(aq))
+        return FP8_ERR_INVALID_ARG;
+    gather_kernel<<<warps_grid(R), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(xq), xs, row_token, R, K, static_cast<uint4*>(aq), as);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" fp8_status fp8_moe_combine(const void* out, const float* w, const int32_t* pair_row,
+                                      int64_t T, int32_t topk, int64_t D, void* y_bf16,
+                                      float* y_fp32, void* stream) {
+    if (T < 0 || topk <= 0 || D <= 0 || D % 8 != 0) return FP8_ERR_INVALID_ARG;
+    if (T == 0) return FP8_OK;
+    if (!out || !w || !pair_row || (!y_bf16 && !y_fp32) || !aligned16(out) ||
+        (y_bf16 && !aligned16(y_bf16)) || (y_fp32 && !aligned16(y_fp32)))
+        return FP8_ERR_INVALID_ARG;
+    combine_kernel<<<warps_grid(T), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(out), w, pair_row, T, topk, D, static_cast<uint4*>(y_bf16),
+        reinterpret_cast<float4*>(y_fp32));
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}

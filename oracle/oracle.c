@@ -66,6 +66,20 @@ double oracle_e4m3_decode(uint8_t code)
     return sign ? -mag : mag;
 }
 
+/* The 256 decoded values, tabulated once from the definition above so the
+ * loops below do not recompute it per element. */
+static double e4m3_table[256];
+static int e4m3_table_ready = 0;
+
+static void e4m3_table_init(void)
+{
+    if (e4m3_table_ready)
+        return;
+    for (int c = 0; c < 256; ++c)
+        e4m3_table[c] = oracle_e4m3_decode((uint8_t)c);
+    e4m3_table_ready = 1;
+}
+
 /* Nearest e4m3 code to v (R3).  The non-negative finite codes 0x00..0x7E
  * are increasing in value, so the answer is one of the two codes that
  * bracket |v|; a tie goes to the code with an even last mantissa bit. */
@@ -75,16 +89,17 @@ uint8_t oracle_e4m3_encode(float v)
     double a = fabs((double)v);
     if (isnan(v))
         return (uint8_t)(sign | 0x7F);
-    if (a >= oracle_e4m3_decode(0x7E))          /* saturate (incl. inf) */
+    e4m3_table_init();
+    if (a >= e4m3_table[0x7E])                  /* saturate (incl. inf) */
         return (uint8_t)(sign | 0x7E);
     /* binary search keeping decode(lo) <= a < decode(hi) */
     int lo = 0, hi = 0x7E;
     while (hi - lo > 1) {
         int mid = (lo + hi) / 2;
-        if (oracle_e4m3_decode((uint8_t)mid) <= a) lo = mid; else hi = mid;
+        if (e4m3_table[mid] <= a) lo = mid; else hi = mid;
     }
-    double below = oracle_e4m3_decode((uint8_t)lo);
-    double above = oracle_e4m3_decode((uint8_t)(lo + 1));
+    double below = e4m3_table[lo];
+    double above = e4m3_table[lo + 1];
     double d_lo = a - below, d_hi = above - a;  /* exact: all dyadic, few bits */
     int code;
     if (d_lo < d_hi) code = lo;
@@ -96,6 +111,7 @@ uint8_t oracle_e4m3_encode(float v)
 /* Array forms of the scalar codec (plain loops, for the tests). */
 void oracle_e4m3_encode_array(const float *v, int64_t n, uint8_t *out)
 {
+    e4m3_table_init();
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_e4m3_encode(v[i]);
@@ -199,6 +215,7 @@ static float block_scale(float amax, int ue8m0)
 void oracle_act_quant(const uint16_t *x, int64_t M, int64_t K, int ue8m0,
                       uint8_t *y, float *s)
 {
+    e4m3_table_init();
     int64_t KB = K / ORACLE_BLOCK;
 #pragma omp parallel for schedule(static)
     for (int64_t m = 0; m < M; ++m) {
@@ -228,6 +245,7 @@ void oracle_act_quant(const uint16_t *x, int64_t M, int64_t K, int ue8m0,
 void oracle_weight_quant(const uint16_t *w, int64_t N, int64_t K, int ue8m0,
                          uint8_t *q, float *s)
 {
+    e4m3_table_init();
     int64_t NB = (N + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
     int64_t KB = (K + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
 #pragma omp parallel for schedule(static)
@@ -261,6 +279,7 @@ void oracle_weight_quant(const uint16_t *w, int64_t N, int64_t K, int ue8m0,
 void oracle_weight_dequant(const uint8_t *w, const float *s, int64_t M, int64_t N,
                            uint16_t *y)
 {
+    e4m3_table_init();
     int64_t NB = (N + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < M; ++i)
@@ -283,13 +302,14 @@ static void gemm_element(const uint8_t *a_row, const float *as_row,
                          const uint8_t *b_row, const float *bs_row, int64_t K,
                          double *ref, double *mag)
 {
+    e4m3_table_init();
     int64_t KB = K / ORACLE_BLOCK;
     double r = 0.0, g = 0.0;
     for (int64_t kb = 0; kb < KB; ++kb) {
         double dot = 0.0, adot = 0.0;
         for (int i = 0; i < ORACLE_BLOCK; ++i) {
-            double p = oracle_e4m3_decode(a_row[kb * ORACLE_BLOCK + i]) *
-                       oracle_e4m3_decode(b_row[kb * ORACLE_BLOCK + i]);
+            double p = e4m3_table[a_row[kb * ORACLE_BLOCK + i]] *
+                       e4m3_table[b_row[kb * ORACLE_BLOCK + i]];
             dot += p;
             adot += fabs(p);
         }
@@ -308,6 +328,7 @@ void oracle_gemm(const uint8_t *a, const float *a_s, const uint8_t *b, const flo
                  int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
                  double *ref, double *mag)
 {
+    e4m3_table_init();
     int64_t KB = K / ORACLE_BLOCK;
     (void)M;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -328,6 +349,7 @@ void oracle_grouped_gemm(const uint8_t *a, const float *a_s, const uint8_t *b,
                          int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
                          double *ref, double *mag)
 {
+    e4m3_table_init();
     int64_t KB = K / ORACLE_BLOCK;
     int64_t NB = (N + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
 #pragma omp parallel for schedule(dynamic, 1)

@@ -1,0 +1,136 @@
+"""GPU parity of fp8_gemm (data-flow page, "FP8 quantization data flow";
+source tour, "FP8 with per-block scales") against the oracle's exact
+block-scaled sum, on the decode (operand-swapped, stream-K), ragged,
+prefill (data-parallel) and tiny workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests.helpers import check_gemm, dev_e4m3, dev_f32, host_bits, host_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import fp8_block_scaled_07_gb300 as m
+    return m
+
+
+def _run(fp8, aq, as_, bq, bs, rows=None, what=""):
+    cb, cf = fp8.fp8_gemm(dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs), out_bf16=True, out_fp32=True)
+    fp8.fp8_device_status()
+    ref, mag = oracle.gemm(aq, as_, bq, bs, rows=rows)
+    cf_h, cb_h = host_f32(cf), host_bits(cb)
+    if rows is not None:
+        cf_h, cb_h = cf_h[rows], cb_h[rows]
+    return check_gemm(ref, mag, cf_h, cb_h, what)
+
+
+def _quantised(lin, ue8m0=False):
+    aq, as_ = oracle.act_quant(lin.x, ue8m0=ue8m0)
+    bq, bs = oracle.weight_quant(lin.w)
+    return aq, as_, bq, bs
+
+
+def test_single_tile_random_codes(fp8):
+    # one 128x16 swapped tile, one slab: the smallest tensor-core path
+    a = syn.random_e4m3_codes((16, 128), 1)
+    b = syn.random_e4m3_codes((128, 128), 2)
+    _run(fp8, a, np.ones((16, 1), np.float32), b, np.ones((1, 1), np.float32), what="single tile")
+
+
+def test_tiny_linear(fp8):
+    _run(fp8, *_quantised(syn.tiny_linear()), what="tiny")
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_decode_linears(fp8, M):
+    for lin in syn.decode_linears(M):
+        _run(fp8, *_quantised(lin), what=f"{lin.name} M={M}")
+
+
+@pytest.mark.parametrize("M", [2, 5, 17, 33, 48])
+def test_decode_odd_batches(fp8, M):
+    lin = syn.decode_linears(M, layers=["wq_a"])[0]
+    _run(fp8, *_quantised(lin), what=f"wq_a M={M}")
+
+
+@pytest.mark.parametrize("M", [37, 2049])
+def test_ragged_n_ue8m0(fp8, M):
+    _run(fp8, *_quantised(syn.ragged_ue8m0(M), ue8m0=True), what=f"wkv_a M={M}")
+
+
+@pytest.mark.parametrize("shape", [(300, 384, 1024), (129, 136, 256), (65, 8, 128), (200, 1000, 384)])
+def test_ragged_non_swapped(fp8, shape):
+    M, N, K = shape
+    a = syn.random_e4m3_codes((M, K), M)
+    b = syn.random_e4m3_codes((N, K), N)
+    as_ = syn.random_scales((M, K // 128), 3)
+    bs = syn.random_scales(((N + 127) // 128, K // 128), 4)
+    _run(fp8, a, as_, b, bs, what=f"ragged {shape}")
+
+
+def test_data_parallel_schedule(fp8):
+    # >= 4 tiles per SM: whole tiles per CTA, no workspace
+    sms = fp8.fp8_num_sms()
+    M, N, K = 2048, 128 * ((4 * sms + 15) // 16), 256
+    assert fp8.fp8_gemm_workspace_size(M, N, K) == 0
+    a = syn.random_e4m3_codes((M, K), 5)
+    b = syn.random_e4m3_codes((N, K), 6)
+    as_ = syn.random_scales((M, K // 128), 7)
+    bs = syn.random_scales(((N + 127) // 128, K // 128), 8)
+    rows = np.r_[0:3, 127:130, 1000, M - 2:M]
+    _run(fp8, a, as_, b, bs, rows=rows, what="data-parallel")
+
+
+def test_prefill_mlp_shapes_sampled(fp8):
+    x = syn.mlp_activations(M=4096)
+    aq, as_ = oracle.act_quant(x)
+    rng = np.random.default_rng(9)
+    rows = np.unique(np.r_[0, 1, 127, 128, 4095, rng.integers(0, 4096, 11)])
+    w1 = syn.mlp_weight("w1", (syn.MLP_INTER, syn.MLP_DIM))
+    bq, bs = oracle.weight_quant(w1)
+    _run(fp8, aq, as_, bq, bs, rows=rows, what="w1 M=4096")
+
+
+def test_workspace_too_small_is_reported(fp8):
+    lin = syn.decode_linears(16, layers=["wq_a"])[0]
+    aq, as_, bq, bs = _quantised(lin)
+    need = fp8.fp8_gemm_workspace_size(16, 1536, 7168)
+    assert need > 0
+    ws = torch.zeros(need // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fp8.Fp8Error) as ei:
+        fp8.fp8_gemm(dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs), workspace=ws)
+    assert ei.value.status == 5
+
+
+def test_repeat_calls_are_deterministic_and_leave_workspace_clean(fp8):
+    lin = syn.decode_linears(16, layers=["wo"])[0]
+    aq, as_, bq, bs = _quantised(lin)
+    need = fp8.fp8_gemm_workspace_size(16, 7168, 16384)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    args = (dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs))
+    outs = [host_f32(fp8.fp8_gemm(*args, out_bf16=False, out_fp32=True, workspace=ws)[1]) for _ in range(3)]
+    fp8.fp8_device_status()
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    # counters region (first 16 KiB) returns to zero
+    cnt = ws[: 16384].view(torch.int32)
+    assert int(cnt.abs().sum()) == 0
+
+
+def test_one_workspace_serves_shapes_in_any_order(fp8):
+    # a call with few split tiles leaves partials where a later call with
+    # more split tiles keeps counters: counters must live apart from partials
+    ws = torch.zeros(fp8.fp8_gemm_workspace_size(16, 24576, 16384), dtype=torch.uint8, device="cuda")
+    for M, name in [(16, "wq_a"), (16, "wo"), (16, "wq_b"), (1, "wq_b"), (16, "wq_a")]:
+        lin = syn.decode_linears(M, layers=[name])[0]
+        aq, as_, bq, bs = _quantised(lin)
+        assert fp8.fp8_gemm_workspace_size(M, *lin.w.shape) <= ws.numel()
+        cb, cf = fp8.fp8_gemm(dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs), out_fp32=True, workspace=ws)
+        fp8.fp8_device_status()
+        ref, mag = oracle.gemm(aq, as_, bq, bs)
+        check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"{name} M={M} shared workspace")
