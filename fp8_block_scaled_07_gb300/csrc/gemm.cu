@@ -38,6 +38,24 @@ namespace fp8bs {
 
 __device__ int g_gemm_status;   // FP8_OK or FP8_ERR_TIMEOUT, read by fp8_device_status
 
+// Optional per-CTA timeline (global timer, ns) for profiling builds only;
+// compiles to nothing unless FP8BS_TRACE_ENABLED is defined.
+#ifdef FP8BS_TRACE_ENABLED
+__device__ unsigned long long g_trace[1024][8];
+#define FP8BS_TRACE(slot)                                                            \
+    do {                                                                             \
+        if (blockIdx.x < 1024) {                                                     \
+            unsigned long long t_;                                                   \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                    \
+            g_trace[blockIdx.x][slot] = t_;                                          \
+        }                                                                            \
+    } while (0)
+#else
+#define FP8BS_TRACE(slot) \
+    do {                  \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int kNumThreads = 256;
@@ -261,6 +279,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) FP8BS_TRACE(0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -302,6 +321,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tc_fence_after();
     if (V == kGrouped) num_tiles = s_prefix[p.G];
     const uint32_t tmem_base = *tmem_holder;
+    if (threadIdx.x == 0) FP8BS_TRACE(1);
 
     SegIter it;
     it.init(p, num_tiles);
@@ -321,6 +341,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (iter == 0) FP8BS_TRACE(2);
                     mbar_arrive_expect_tx(&full[st], C::kStageBytes);
                     tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
                     tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
@@ -350,6 +371,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (iter == 0) FP8BS_TRACE(3);
                     const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
                     const uint64_t da = smem_desc_sw128(smem_u32(sP + st * kPTileBytes));
                     const uint64_t db = smem_desc_sw128(smem_u32(sQ + st * C::kQTileBytes));
@@ -407,6 +429,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                if (slab == 0 && e == 0) FP8BS_TRACE(4);
                 const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
                 if constexpr (BN == 16) {
                     uint32_t r[16];
@@ -431,6 +454,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 mbar_arrive(&tempty[buf]);
             }
             if (!ok) break;
+            if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
                 store_tile<BN, V>(p, tg, e, acc);
                 continue;
@@ -468,6 +492,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 store_tile<BN, V>(p, tg, e, acc);
                 if (e == 0) p.counters[sg.tile] = 0;
             }
+            if (e == 0) FP8BS_TRACE(6);
         }
     }
 
@@ -475,6 +500,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+    if (threadIdx.x == 0) FP8BS_TRACE(7);
 }
 
 // ------------------------------------------------------------------ host side
@@ -584,6 +610,13 @@ int gemm_read_and_clear_status(cudaStream_t st) {
 }  // namespace fp8bs
 
 using namespace fp8bs;
+
+#ifdef FP8BS_TRACE_ENABLED
+extern "C" int fp8_debug_read_trace(unsigned long long* host, int n_ctas) {
+    if (n_ctas > 1024) n_ctas = 1024;
+    return cudaMemcpyFromSymbol(host, g_trace, static_cast<size_t>(n_ctas) * 8 * 8) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 extern "C" size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kBlock != 0) return 0;
