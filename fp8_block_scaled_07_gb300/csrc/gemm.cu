@@ -712,3 +712,57 @@ extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const vo
                                           static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------ no-allocation variant
+// Some callers cannot allocate device memory at the point where they run a
+// linear layer: code that must not call cudaMalloc (which can synchronise the
+// device) on a latency-critical path, code running under a fixed memory
+// budget, or hosts that own the CUDA allocator and hand out no scratch.  For
+// them fp8_gemm_noalloc runs fp8_gemm with the split-tile scratch taken from
+// a fixed array that lives in this library's device image.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB per device, held until exit
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// The array's name is only a host-side stand-in; its device address is looked
+// up once per device (with that device current) and cached here.
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {nullptr};
+
+fp8_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return FP8_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const void* b,
+                                       const float* b_s, void* c_bf16, float* c_fp32, int64_t M,
+                                       int64_t N, int64_t K, void* stream) {
+    if (M < 0 || N < 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    const size_t need = fp8_gemm_workspace_size(M, N, K);
+    if (need > kNoAllocScratchBytes) return FP8_ERR_WORKSPACE;   // beyond the fixed array
+    void* scratch = nullptr;
+    if (need > 0) {
+        const fp8_status st = noalloc_scratch(&scratch);
+        if (st != FP8_OK) return st;
+        // the split-tile counters must start at zero; the array keeps whatever
+        // the previous call (or an aborted one) left in it
+        if (cudaMemsetAsync(scratch, 0, kCounterBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FP8_ERR_CUDA;
+    }
+    return fp8_gemm(a, a_s, b, b_s, c_bf16, c_fp32, M, N, K, scratch, need > 0 ? kNoAllocScratchBytes : 0,
+                    stream);
+}

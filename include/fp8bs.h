@@ -104,6 +104,28 @@ fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float*
                     void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* fp8_gemm without any allocation (the paper has no counterpart: this is a
+ * convenience of this library).  For callers that cannot hand the library a
+ * workspace -- code that must not call cudaMalloc on its hot path (it can
+ * synchronise the device), code under a fixed memory budget, or hosts whose
+ * allocator gives out no scratch.  Same arguments and result as fp8_gemm,
+ * minus the workspace: the split-tile scratch comes from a fixed 8 MiB
+ * (8388608-byte) device array inside the library, held on every GPU that
+ * loads the library until the process exits.
+ *   - The first call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture.
+ *   - Shapes whose split-K schedule needs more scratch than the array holds
+ *     (fp8_gemm_workspace_size(M, N, K) > 8 MiB) return FP8_ERR_WORKSPACE and
+ *     launch nothing; use fp8_gemm with a caller workspace for those.
+ *   - Every call clears the counters it needs on `stream` and then uses the
+ *     shared array: calls that may overlap on the GPU (different streams,
+ *     different host threads) race on it and must be serialised by the
+ *     caller.  No cudaMalloc, cudaFree or allocating routine is called. */
+fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const void* b, const float* b_s,
+                            void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
+                            void* stream);
+
 /* Grouped fp8_gemm over routed experts (behavior-traces page, "MoE trace";
  * source tour, "Honest Limits").  Expert g owns the packed activation rows
  * [offsets[g], offsets[g+1]) of a [R_max, K] (e4m3, scales a_s [R_max,

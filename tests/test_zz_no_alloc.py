@@ -1,0 +1,83 @@
+"""fp8_gemm_noalloc: the GEMM for callers that cannot give the library a
+workspace (no cudaMalloc allowed on their path, a fixed memory budget, or an
+allocator that hands out no scratch).  Its split-tile scratch is a fixed
+8 MiB array inside the library, so the result must match fp8_gemm with a
+caller workspace, and two calls in a row (the second finding the first
+one's leftovers in the shared array) must both be right.
+
+Called through the C ABI with ctypes.  Kept in its own file, collected last."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests.helpers import check_gemm, dev_e4m3, dev_f32, host_bits, host_f32
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 8 << 20
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import fp8_block_scaled_07_gb300 as m
+    f = m.lib.fp8_gemm_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+    return m
+
+
+def _p(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _noalloc(fp8, a, a_s, b, b_s, M, N, K):
+    cb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    cf = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    st = fp8.lib.fp8_gemm_noalloc(_p(a), _p(a_s), _p(b), _p(b_s), _p(cb), _p(cf), M, N, K,
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st, cb, cf
+
+
+def _case(name, M):
+    lin = syn.decode_linears(M, layers=[name])[0]
+    aq, as_ = oracle.act_quant(lin.x)
+    bq, bs = oracle.weight_quant(lin.w)
+    return aq, as_, bq, bs
+
+
+def test_two_calls_in_a_row_match_the_workspace_entry_point(fp8):
+    cases = [("wo", 16), ("wq_a", 16)]          # both split K across CTAs (use scratch)
+    results = []
+    for name, M in cases:
+        aq, as_, bq, bs = _case(name, M)
+        N, K = syn.DECODE_LAYERS[name]
+        assert 0 < fp8.fp8_gemm_workspace_size(M, N, K) <= SCRATCH_BYTES
+        args = (dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs))
+        st, cb, cf = _noalloc(fp8, *args, M, N, K)
+        assert st == 0, fp8.lib.fp8_status_string(st)
+        results.append((name, M, aq, as_, bq, bs, args, cb, cf))
+    fp8.fp8_device_status()
+    for name, M, aq, as_, bq, bs, args, cb, cf in results:
+        ref, mag = oracle.gemm(aq, as_, bq, bs)
+        check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"noalloc {name} M={M}")
+        wb, wf = fp8.fp8_gemm(*args, out_bf16=True, out_fp32=True)
+        fp8.fp8_device_status()
+        diff = np.abs(host_f32(cf).astype(np.float64) - host_f32(wf))
+        assert np.all(diff <= 1e-4 * mag), f"{name}: noalloc differs from fp8_gemm"
+
+
+def test_shapes_needing_more_scratch_are_rejected(fp8):
+    M, (N, K) = 64, syn.DECODE_LAYERS["wq_a"]
+    if fp8.fp8_gemm_workspace_size(M, N, K) <= SCRATCH_BYTES:
+        pytest.skip("this device's schedule fits the fixed scratch")
+    a = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    s = torch.ones((M, K // 128), dtype=torch.float32, device="cuda")
+    b = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    bs = torch.ones((N // 128, K // 128), dtype=torch.float32, device="cuda")
+    st, _, _ = _noalloc(fp8, a, s, b, bs, M, N, K)
+    assert st == 5   # FP8_ERR_WORKSPACE: nothing launched
