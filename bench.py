@@ -14,8 +14,9 @@ value  = algorithmic HBM bytes of the step / device time (GB/s); the
 e2e    = same metric through the Python binding with host buffers: each
          step copies the activations host->device, runs the six calls and
          copies the outputs device->host;
-roofline = the fp8_gemm kernel alone (the dominant kernel), per-launch
-         CUDA-event durations taken inside the timed graphs;
+roofline = the fp8_gemm kernel alone (the dominant kernel): per-launch
+         CUDA-event durations of graphs that replay only that layer's GEMM
+         (four weight rotations), taken right after the timed region;
 cpu_baseline = the CPU oracle on the host cores over a bounded sample.
 
 With --impl reference the CPU oracle itself is timed on the same workload
@@ -186,26 +187,13 @@ class Decode:
         self.ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
-    def step(self, r, x=None, events=None):
+    def step(self, r, x=None):
         fp8 = self.fp8
         xs = self.x[r] if x is None else x
-        for i, name in enumerate(LAYERS):
+        for name in LAYERS:
             wq, wsc = self.w[r][name]
             fp8.fp8_act_quant(xs[name], y=self.xq[name], s=self.xs[name])
-            if events is not None:
-                events[i][0].record()
             fp8.fp8_gemm(self.xq[name], self.xs[name], wq, wsc, c_bf16=self.y[name], workspace=self.ws)
-            if events is not None:
-                events[i][1].record()
-
-
-def make_event(torch, external):
-    if external:
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return None
-    return torch.cuda.Event(enable_timing=True)
 
 
 def capture(torch, fn):
@@ -331,35 +319,24 @@ def rows_measurements(fp8, torch, peaks):
     gq = torch.empty((M, I), dtype=torch.float8_e4m3fn, device=dev)
     gsc = torch.empty((M, I // 128), dtype=torch.float32, device=dev)
     yv = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
-    ev = [make_event(torch, True) for _ in range(4)]
-    ext = all(e is not None for e in ev)
-
     def mlp():
         fp8.fp8_act_quant(x, y=xq, s=xs)
-        if ext:
-            ev[0].record()
         fp8.fp8_gemm(xq, xs, w13q, w13s, c_bf16=h13)
-        if ext:
-            ev[1].record()
         fp8.fp8_silu_mul_quant(h13, h13[:, I:], 2 * I, M, I, y=gq, s=gsc)
-        if ext:
-            ev[2].record()
         fp8.fp8_gemm(gq, gsc, w2q, w2s, c_bf16=yv)
-        if ext:
-            ev[3].record()
     g = capture(torch, mlp)
     ms = time_graph(torch, g, 10)
     flops = 3 * gemm_flops(M, I, D)
     row = {"workload": "dense MLP M=4096, 7168->2x18432->7168", "ms": ms, "TFLOP/s": flops / ms / 1e9,
            "frac_fp8_peak": flops / ms / 1e9 / fp8_peak}
-    if ext:
-        g.replay()
-        torch.cuda.synchronize()
-        t13, t2 = ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3])
-        f13, f2 = gemm_flops(M, 2 * I, D), gemm_flops(M, D, I)
-        row["gemm_w13"] = {"ms": t13, "TFLOP/s": f13 / t13 / 1e9, "frac_fp8_peak": f13 / t13 / 1e9 / fp8_peak}
-        row["gemm_w2"] = {"ms": t2, "TFLOP/s": f2 / t2 / 1e9, "frac_fp8_peak": f2 / t2 / 1e9 / fp8_peak}
+    g13 = capture(torch, lambda: fp8.fp8_gemm(xq, xs, w13q, w13s, c_bf16=h13))
+    g2 = capture(torch, lambda: fp8.fp8_gemm(gq, gsc, w2q, w2s, c_bf16=yv))
+    t13, t2 = time_graph(torch, g13, 10), time_graph(torch, g2, 10)
+    f13, f2 = gemm_flops(M, 2 * I, D), gemm_flops(M, D, I)
+    row["gemm_w13"] = {"ms": t13, "TFLOP/s": f13 / t13 / 1e9, "frac_fp8_peak": f13 / t13 / 1e9 / fp8_peak}
+    row["gemm_w2"] = {"ms": t2, "TFLOP/s": f2 / t2 / 1e9, "frac_fp8_peak": f2 / t2 / 1e9 / fp8_peak}
     out["prefill_mlp"] = row
+    del g13, g2
     del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv, g
 
     # MoE: 4096 tokens x top-8 of 256 experts (Zipf), w1|w3 [4096, 7168], w2 [7168, 2048] per expert
@@ -386,17 +363,10 @@ def rows_measurements(fp8, torch, peaks):
         off, pr, rtok = fp8.fp8_moe_route(ids, E)
         fp8.fp8_act_quant(x, y=xq, s=xs)
         aq, as_ = fp8.fp8_moe_gather(xq, xs, rtok)
-        if ext:
-            ev[0].record()
         h, _ = fp8.fp8_grouped_gemm(aq, as_, w13q, w13s, off)
-        if ext:
-            ev[1].record()
         gq_, gs_, _ = fp8.fp8_silu_mul_quant(h, h[:, I:], 2 * I, R, I)
-        if ext:
-            ev[2].record()
         o2, _ = fp8.fp8_grouped_gemm(gq_, gs_, w2q, w2s, off)
-        if ext:
-            ev[3].record()
+        st.update(off=off, aq=aq, as_=as_, h=h, gq=gq_, gs=gs_, o2=o2)
         st["y"] = fp8.fp8_moe_combine(o2, wts, pr)[0]
     g = capture(torch, moe)
     ms = time_graph(torch, g, 5)
@@ -405,12 +375,12 @@ def rows_measurements(fp8, torch, peaks):
     row = {"workload": "MoE 4096 tok x top-8 of 256, 7168->2x2048->7168", "ms": ms,
            "TFLOP/s": flops / ms / 1e9, "weight_GB/s": wbytes / ms / 1e6,
            "roofline_ms": max(wbytes / hbm / 1e6, flops / fp8_peak / 1e9)}
-    if ext:
-        g.replay()
-        torch.cuda.synchronize()
-        row["grouped_w13_ms"] = ev[0].elapsed_time(ev[1])
-        row["grouped_w2_ms"] = ev[2].elapsed_time(ev[3])
+    g13 = capture(torch, lambda: fp8.fp8_grouped_gemm(st["aq"], st["as_"], w13q, w13s, st["off"], c_bf16=st["h"]))
+    g2 = capture(torch, lambda: fp8.fp8_grouped_gemm(st["gq"], st["gs"], w2q, w2s, st["off"], c_bf16=st["o2"]))
+    row["grouped_w13_ms"] = time_graph(torch, g13, 5)
+    row["grouped_w2_ms"] = time_graph(torch, g2, 5)
     out["moe"] = row
+    del g13, g2
     del w13q, w2q, g
     torch.cuda.empty_cache()
     return out
@@ -501,11 +471,9 @@ def main():
     dec = Decode(fp8, torch)
     M = dec.M
 
-    # graphs: one per weight rotation, with external timing events around each GEMM
-    events = [[[make_event(torch, True), make_event(torch, True)] for _ in LAYERS] for _ in range(dec.R)]
-    have_ev = all(e is not None for r in events for l in r for e in l)
-    graphs = [capture(torch, lambda r=r: dec.step(r, events=events[r] if have_ev else None))
-              for r in range(dec.R)]
+    # one graph per weight rotation; nothing but the six kernels, so the
+    # programmatic launch edges between consecutive kernels stay intact
+    graphs = [capture(torch, lambda r=r: dec.step(r)) for r in range(dec.R)]
     for i in range(args.warmup):
         graphs[i % dec.R].replay()
     torch.cuda.synchronize()
@@ -531,17 +499,23 @@ def main():
     ms = t_start.elapsed_time(t_end)
     fp8.fp8_device_status()
 
-    # per-launch GEMM durations from the last replay of every rotation graph
-    gemm_ms, gemm_b = 0.0, 0
-    per_layer = {}
-    if have_ev:
-        for r in range(dec.R):
-            for i, name in enumerate(LAYERS):
-                t = events[r][i][0].elapsed_time(events[r][i][1])
-                gemm_ms += t
-                N, K = syn.DECODE_LAYERS[name]
-                gemm_b += gemm_bytes(M, N, K)
-                per_layer.setdefault(name, []).append(t)
+    # per-launch fp8_gemm durations: per layer, a graph of its GEMM over the
+    # four weight rotations (inputs already quantised), events around replays
+    gemm_ms, gemm_b, per_layer = 0.0, 0, {}
+    for name in LAYERS:
+        N, K = syn.DECODE_LAYERS[name]
+
+        def gemms(name=name):
+            for r in range(dec.R):
+                wq, wsc = dec.w[r][name]
+                fp8.fp8_gemm(dec.xq[name], dec.xs[name], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
+        g = capture(torch, gemms)
+        t = time_graph(torch, g, 50) / dec.R
+        per_layer[name] = t
+        gemm_ms += t
+        gemm_b += gemm_bytes(M, N, K)
+        del g
+    have_ev = gemm_ms > 0
 
     ms_max = ms
     if pg:
@@ -609,7 +583,8 @@ def main():
                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                             "peak_kind": f"{peak_src} copy bandwidth",
                             "traffic": profiled_traffic("fp8_gemm", "decode_M16"),
-                            "launch_us": {n: float(np.mean(v)) * 1e3 for n, v in per_layer.items()}}
+                            "launch_us": {n: v * 1e3 for n, v in per_layer.items()},
+                            "timing": "per layer: CUDA graph of its 4 rotation launches, events around 50 replays"}
     if rank == 0 and world == 1 and not args.no_cpu:
         secs, nb, fl = oracle_decode_sample(torch, dec, 16)
         line["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": omp_threads(), "kind": "oracle",

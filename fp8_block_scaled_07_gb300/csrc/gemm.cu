@@ -69,6 +69,7 @@ constexpr int kMaxSkTiles = 4096;
 constexpr size_t kCounterBytes = kMaxSkTiles * sizeof(int);
 
 enum Variant { kDense = 0, kDenseSwap = 1, kGrouped = 2 };
+constexpr int kScaleChunk = 32;   // slabs of scale products staged at a time (swapped layout)
 
 struct Params {
     const float* a_s;          // [rows_a, KB]
@@ -100,15 +101,23 @@ struct Seg {
     int tile, k0, k1;
 };
 
-template <int BN>
+template <int BN, int V>
 struct Cfg {
+    static constexpr bool kSwap = (V == kDenseSwap);
     static constexpr int kQTileBytes = BN * kBlock;
     static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
-    static constexpr int kStages = BN >= 128 ? 6 : 8;
+    // small swapped tiles: 5 stages (80 KB of weights in flight) so that two
+    // CTAs fit on an SM -- the next launch's CTAs start while this one drains
+    static constexpr int kStages = (kSwap && BN <= 32) ? 5 : (BN >= 128 ? 6 : 8);
+    static constexpr int kMinBlocks = (kSwap && BN <= 32) ? 2 : 1;
     static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,32,64,128}
     static constexpr int kBarBytes = 1024;
-    static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes +
-                                      (kMaxGroups + 1) * 4;
+    // grouped: per-expert tile prefix; swapped: two chunks of staged scales
+    static constexpr int kExtraBytes =
+        V == kGrouped ? (kMaxGroups + 1) * 4 : (kSwap ? 2 * kScaleChunk * BN * 4 : 0);
+    static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes + kExtraBytes;
+    // weight slabs each CTA prefetches into L2 before its inputs are ready
+    static constexpr int kL2Prefetch = kStages;
 };
 
 // ------------------------------------------------------------------ schedule
@@ -255,11 +264,48 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
     }
 }
 
+// Promote one finished slab from TMEM into the fp32 accumulators:
+// acc[j] += D[lane][j] * scale, the scale per column (smem, swapped layout)
+// or uniform for the row.
+template <int BN, bool PER_COL>
+__device__ __forceinline__ void promote(uint32_t taddr, float (&acc)[BN], const float* sc_col, float sc) {
+    if constexpr (BN == 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = fmaf(__uint_as_float(r[j]), PER_COL ? sc_col[j] : sc, acc[j]);
+    } else {
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                acc[c0 + j] = fmaf(__uint_as_float(r[j]), PER_COL ? sc_col[c0 + j] : sc, acc[c0 + j]);
+        }
+    }
+}
+
+// Barrier of the 128 epilogue threads on an mbarrier (count 128) so that a
+// thread that gave up on a wait cannot leave the others blocked forever.
+__device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const volatile int* abort_flag) {
+    mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase, abort_flag);
+    phase ^= 1u;
+    if (!ok) {
+        *const_cast<volatile int*>(abort_flag) = 1;
+        atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_TIMEOUT));
+    }
+    return ok;
+}
+
 template <int BN, int V>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
     gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
                 const Params p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, V>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -272,14 +318,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint64_t* tfull = bars + 2 * S;        // 2
     uint64_t* tempty = bars + 2 * S + 2;   // 2
     uint64_t* mma_done = bars + 2 * S + 4; // 1
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    uint64_t* epi_bar = bars + 2 * S + 5;  // epilogue-group barrier
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
     int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kBarBytes);
+    float* s_scale = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kBarBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) FP8BS_TRACE(0);
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -291,17 +340,34 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             mbar_init(&tempty[i], 128);
         }
         mbar_init(mma_done, 1);
+        mbar_init(epi_bar, 128);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_p);
         tma_prefetch_desc(&tm_q);
+        if constexpr (V != kGrouped) {
+            // start streaming this CTA's first weight slabs into L2 while the
+            // producer of the activations may still be running
+            SegIter pit;
+            pit.init(p, p.num_tiles);
+            Seg ps;
+            int n = 0;
+            while (n < C::kL2Prefetch && pit.next(ps)) {
+                const Tile tg = tile_geom<BN, V>(p, ps.tile, nullptr);
+                for (int kb = ps.k0; kb < ps.k1 && n < C::kL2Prefetch; ++kb, ++n) {
+                    if (V == kDenseSwap) tma_prefetch_l2_2d(&tm_p, kb * kBlock, tg.p_row0);
+                    else tma_prefetch_l2_2d(&tm_q, kb * kBlock, tg.q_row0);
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, C::kTmemCols);
         tmem_relinquish();
     }
+    griddep_wait();   // inputs written by earlier launches are visible from here on
     int num_tiles = p.num_tiles;
     if (V == kGrouped) {
         // exclusive prefix over experts of (m-tiles x n-tiles)
@@ -391,67 +457,92 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const int q = warp & 3;                     // TMEM lane quarter
         const int e = q * 32 + lane;                // row of the tile (TMEM lane)
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t slab = 0;
+        uint32_t slab = 0, epi_phase = 0, chunk_ctr = 0;
         bool ok = true;
+        // one finished slab: wait for it in TMEM, promote it, free the buffer
+        auto take_slab = [&](float (&acc)[BN], const float* sc_col, float sc) -> bool {
+            const int buf = slab & 1;
+            if (!mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag)) {
+                set_abort(abort_flag);
+                return false;
+            }
+            tc_fence_after();
+            if (slab == 0 && e == 0) FP8BS_TRACE(4);
+            promote<BN, V == kDenseSwap>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN), acc,
+                                         sc_col, sc);
+            tc_fence_before();
+            mbar_arrive(&tempty[buf]);
+            ++slab;
+            return true;
+        };
         while (ok && it.next(sg)) {
             const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
             float acc[BN];
 #pragma unroll
             for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
-            // scale pointers
-            const float* ps;   // per-row (non-swap) / per-block (swap) scale of the P side
-            const float* qs;   // per-block (non-swap) / per-token (swap) scale of the Q side
-            if (V == kDenseSwap) {
-                ps = p.b_s + static_cast<int64_t>(tg.p_row0 / 128) * p.KB;
-                qs = p.a_s + static_cast<int64_t>(tg.q_row0) * p.KB;
-            } else if (V == kDense) {
-                ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
-                qs = p.b_s + static_cast<int64_t>(tg.q_row0 / 128) * p.KB;
-            } else {
-                ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
-                qs = p.b_s + (static_cast<int64_t>(tg.group) * p.NB + tg.q_col0 / 128) * p.KB;
-            }
-            for (int kb = sg.k0; kb < sg.k1; ++kb, ++slab) {
-                const int buf = slab & 1;
-                // scales of this slab (loaded before the wait to hide latency)
-                float sc[V == kDenseSwap ? BN : 1];
-                if constexpr (V == kDenseSwap) {
-                    const float sp = __ldg(ps + kb);
+            if constexpr (V == kDenseSwap) {
+                // scale products b_s[block] * a_s[token] of 32 slabs at a time,
+                // staged in shared memory one chunk ahead
+                constexpr int CH = kScaleChunk, PER = CH * BN / 128;
+                const float* ps = p.b_s + static_cast<int64_t>(tg.p_row0 / 128) * p.KB;
+                const float* qs = p.a_s + static_cast<int64_t>(tg.q_row0) * p.KB;
+                float pre[PER];
+                auto issue = [&](int base) {
 #pragma unroll
-                    for (int j = 0; j < BN; ++j)
-                        sc[j] = j < tg.q_valid ? sp * __ldg(qs + static_cast<int64_t>(j) * p.KB + kb) : 0.0f;
-                } else {
-                    sc[0] = __ldg(ps + kb) * __ldg(qs + kb);
-                }
-                if (!mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag)) {
-                    set_abort(abort_flag);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (slab == 0 && e == 0) FP8BS_TRACE(4);
-                const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(buf * BN);
-                if constexpr (BN == 16) {
-                    uint32_t r[16];
-                    tmem_ld16(taddr, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        acc[j] = fmaf(__uint_as_float(r[j]), sc[V == kDenseSwap ? j : 0], acc[j]);
-                } else {
-#pragma unroll
-                    for (int c0 = 0; c0 < BN; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + c0, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[c0 + j] = fmaf(__uint_as_float(r[j]),
-                                               sc[V == kDenseSwap ? c0 + j : 0], acc[c0 + j]);
+                    for (int r = 0; r < PER; ++r) {
+                        const int idx = e + r * 128, i = idx / BN, j = idx % BN, kb = base + i;
+                        pre[r] = (kb < sg.k1 && j < tg.q_valid)
+                                     ? __ldg(ps + kb) * __ldg(qs + static_cast<int64_t>(j) * p.KB + kb)
+                                     : 0.0f;
                     }
+                };
+                auto commit = [&]() {
+                    float* dst = s_scale + (chunk_ctr & 1) * (CH * BN);
+#pragma unroll
+                    for (int r = 0; r < PER; ++r) dst[e + r * 128] = pre[r];
+                };
+                const int n = sg.k1 - sg.k0;
+                issue(sg.k0);
+                for (int rel = 0; rel < n && ok; ++rel) {
+                    const int i = rel % CH;
+                    if (i == 0) {
+                        if (rel > 0) ++chunk_ctr;
+                        commit();
+                        ok = epi_sync(epi_bar, epi_phase, abort_flag);
+                        if (!ok) break;
+                        if (rel + CH < n) issue(sg.k0 + rel + CH);
+                    }
+                    ok = take_slab(acc, s_scale + (chunk_ctr & 1) * (CH * BN) + i * BN, 0.0f);
                 }
-                tc_fence_before();
-                mbar_arrive(&tempty[buf]);
+                ++chunk_ctr;
+            } else {
+                // per-row a_s and per-block b_s, prefetched 8 slabs ahead in registers
+                const float* ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
+                const float* qs = (V == kDense)
+                                      ? p.b_s + static_cast<int64_t>(tg.q_row0 / 128) * p.KB
+                                      : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + tg.q_col0 / 128) * p.KB;
+                float cs[8], na[8], nb[8];
+                auto load8 = [&](int base) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int kb = base + i;
+                        na[i] = kb < sg.k1 ? __ldg(ps + kb) : 0.0f;
+                        nb[i] = kb < sg.k1 ? __ldg(qs + kb) : 0.0f;
+                    }
+                };
+                load8(sg.k0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cs[i] = na[i] * nb[i];
+                load8(sg.k0 + 8);
+                for (int kc = sg.k0; kc < sg.k1 && ok; kc += 8) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (ok && kc + i < sg.k1) ok = take_slab(acc, nullptr, cs[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) cs[i] = na[i] * nb[i];
+                    load8(kc + 16);
+                }
             }
             if (!ok) break;
             if (e == 0) FP8BS_TRACE(5);
@@ -471,23 +562,52 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int which = (first_tile == sg.tile) ? 0 : 1;
                 return p.partials + (static_cast<int64_t>(c) * 2 + which) * (128 * BN);
             };
-            float* mine = slot_of(blockIdx.x);
+            // partial tile layout: [row e][BN columns], 16-byte vectors per thread
+            float* mine = slot_of(blockIdx.x) + e * BN;
 #pragma unroll
-            for (int j = 0; j < BN; ++j) __stcg(mine + j * 128 + e, acc[j]);
+            for (int j = 0; j < BN; j += 4)
+                __stcg(reinterpret_cast<float4*>(mine + j), make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
             __threadfence();
-            named_bar_sync(1, 128);
+            if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
             if (e == 0) *ticket_box = atomicAdd(p.counters + sg.tile, 1);
-            named_bar_sync(1, 128);
+            if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
             const int ticket = *ticket_box;
-            named_bar_sync(1, 128);
+            if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
             if (ticket == nseg - 1) {
                 __threadfence();
 #pragma unroll
                 for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
-                for (int si = 0; si < nseg; ++si) {
-                    const float* src = slot_of(c_first + si);
+                // fixed summation order (segment 0, 1, ...): deterministic; each
+                // batch keeps 8-16 vector loads in flight before adding them
+                constexpr int kFloats = BN <= 32 ? 32 : 64; // floats in flight per thread
+                constexpr int CW = BN < kFloats ? BN : kFloats;   // columns per chunk
+                constexpr int SB = kFloats / CW;                   // segments per batch
 #pragma unroll
-                    for (int j = 0; j < BN; ++j) acc[j] += __ldcg(src + j * 128 + e);
+                for (int c0 = 0; c0 < BN; c0 += CW) {
+                    for (int s0 = 0; s0 < nseg; s0 += SB) {
+                        float4 v[SB][CW / 4];
+#pragma unroll
+                        for (int b = 0; b < SB; ++b) {
+                            if (s0 + b < nseg) {
+                                const float4* src = reinterpret_cast<const float4*>(
+                                    slot_of(c_first + s0 + b) + e * BN + c0);
+#pragma unroll
+                                for (int j = 0; j < CW / 4; ++j) v[b][j] = __ldcg(src + j);
+                            }
+                        }
+#pragma unroll
+                        for (int b = 0; b < SB; ++b) {
+                            if (s0 + b < nseg) {
+#pragma unroll
+                                for (int j = 0; j < CW / 4; ++j) {
+                                    acc[c0 + 4 * j] += v[b][j].x;
+                                    acc[c0 + 4 * j + 1] += v[b][j].y;
+                                    acc[c0 + 4 * j + 2] += v[b][j].z;
+                                    acc[c0 + 4 * j + 3] += v[b][j].w;
+                                }
+                            }
+                        }
+                    }
                 }
                 store_tile<BN, V>(p, tg, e, acc);
                 if (e == 0) p.counters[sg.tile] = 0;
@@ -565,8 +685,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
         pl.ws_bytes = 0;
     } else {
         pl.stream_k = 1;
-        // at least 2 slabs per CTA so the pipeline has something to overlap
+        // at least 2 slabs per CTA so the pipeline has something to overlap,
+        // and at most ~8 CTAs sharing one tile so its reduction stays short
         long long g = std::min<long long>(sms, std::max<long long>(1, pl.total_units / 2));
+        g = std::min<long long>(g, std::max<long long>(1, 8LL * pl.num_tiles));
         pl.grid = static_cast<int>(g);
         pl.counters_bytes = kCounterBytes;
         pl.ws_bytes = pl.counters_bytes + static_cast<size_t>(pl.grid) * 2 * 128 * pl.bn * 4;
@@ -577,7 +699,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
 template <int BN, int V>
 cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& prm, int grid,
                    cudaStream_t st) {
-    constexpr int smem = Cfg<BN>::kSmemBytes;
+    constexpr int smem = Cfg<BN, V>::kSmemBytes;
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -587,8 +709,7 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& p
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    gemm_kernel<BN, V><<<grid, kNumThreads, smem, st>>>(mp, mq, prm);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<BN, V>, dim3(grid), dim3(kNumThreads), smem, st, mp, mq, prm);
 }
 
 }  // namespace

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t* __r
                                                               int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ pair_row,
                                                               int32_t* __restrict__ row_token) {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ int warp_cnt[kRouteThreads / 32];
     __shared__ int warp_lt[kRouteThreads / 32];
     __shared__ int s_base;
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
                                                     const int32_t* __restrict__ row_token,
                                                     int64_t R, int64_t K, uint4* __restrict__ aq,
                                                     float* __restrict__ as) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -94,6 +98,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                                                      int64_t T, int32_t topk, int64_t D,
                                                      uint4* __restrict__ y_bf16,
                                                      float4* __restrict__ y_fp32) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;

@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
                                                              uint2* __restrict__ y,
                                                              float* __restrict__ s,
                                                              int64_t nblocks) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
     const int sub = lane & 15;
@@ -104,6 +106,8 @@ __global__ void __launch_bounds__(kThreads) weight_quant_kernel(const uint16_t* 
                                                                 float* __restrict__ s,
                                                                 int64_t N, int64_t K,
                                                                 int64_t KB) {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ float red[kThreads / 32];
     const int64_t nb = blockIdx.y, kb = blockIdx.x;
     const int chunk = threadIdx.x & 15;
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(kThreads) weight_dequant_kernel(const uint4* _
                                                                   uint4* __restrict__ y,
                                                                   int64_t M, int64_t N,
                                                                   int64_t NB) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t chunks_per_row = N / 16;
     const int64_t total = M * chunks_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -186,6 +192,8 @@ template <bool UE8M0>
 __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(
     const uint16_t* __restrict__ h1, const uint16_t* __restrict__ h3, int64_t ld_h, int64_t R,
     int64_t I, uint2* __restrict__ y, float* __restrict__ s, uint4* __restrict__ g_out) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
     const int sub = lane & 15;
@@ -263,11 +271,9 @@ extern "C" fp8_status fp8_act_quant(const void* x, void* y, float* s, int64_t M,
     const int grid = grid_for(nblocks, (kThreads / 32) * 2 * kUnroll);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (scale_fmt == FP8_SCALE_UE8M0)
-        act_quant_kernel<true><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint4*>(x), static_cast<uint2*>(y), s, nblocks);
+        launch_pdl(act_quant_kernel<true>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint4*>(x), static_cast<uint2*>(y), s, nblocks);
     else
-        act_quant_kernel<false><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint4*>(x), static_cast<uint2*>(y), s, nblocks);
+        launch_pdl(act_quant_kernel<false>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint4*>(x), static_cast<uint2*>(y), s, nblocks);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -282,11 +288,9 @@ extern "C" fp8_status fp8_weight_quant(const void* w, void* q, float* s, int64_t
     dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (scale_fmt == FP8_SCALE_UE8M0)
-        weight_quant_kernel<true><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t*>(w), static_cast<uint8_t*>(q), s, N, K, KB);
+        launch_pdl(weight_quant_kernel<true>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t*>(w), static_cast<uint8_t*>(q), s, N, K, KB);
     else
-        weight_quant_kernel<false><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t*>(w), static_cast<uint8_t*>(q), s, N, K, KB);
+        launch_pdl(weight_quant_kernel<false>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t*>(w), static_cast<uint8_t*>(q), s, N, K, KB);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -317,12 +321,10 @@ extern "C" fp8_status fp8_silu_mul_quant(const void* h1, const void* h3, int64_t
     const int grid = grid_for(nblocks, (kThreads / 32) * 4);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (scale_fmt == FP8_SCALE_UE8M0)
-        silu_mul_quant_kernel<true><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t*>(h1), static_cast<const uint16_t*>(h3), ld_h, R, I,
+        launch_pdl(silu_mul_quant_kernel<true>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t*>(h1), static_cast<const uint16_t*>(h3), ld_h, R, I,
             static_cast<uint2*>(y), s, static_cast<uint4*>(g_bf16));
     else
-        silu_mul_quant_kernel<false><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t*>(h1), static_cast<const uint16_t*>(h3), ld_h, R, I,
+        launch_pdl(silu_mul_quant_kernel<false>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t*>(h1), static_cast<const uint16_t*>(h3), ld_h, R, I,
             static_cast<uint2*>(y), s, static_cast<uint4*>(g_bf16));
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
