@@ -253,14 +253,31 @@ def time_graph(torch, g, iters):
     return s.elapsed_time(e) / iters
 
 
-def rows_measurements(fp8, torch, peaks):
+def rows_measurements(fp8, torch, peaks, only=None):
     """Every other hot-path row on its own workload (device time)."""
+    def want(name):
+        return only is None or name in only
     dev = torch.device("cuda")
     hbm = peaks["hbm_gbs"]
     fp8_peak = 2.0 * peaks["bf16_tflops"]           # dense fp8 = 2x dense bf16 (nominal ratio)
     out = {}
 
     # act_quant alone, prefill-sized input larger than L2 (4096 x 18432 bf16 = 151 MB)
+    if want("act_quant"):
+        act_quant_row(fp8, torch, dev, hbm, out)
+    if want("weight_dequant"):
+        dequant_row(fp8, torch, dev, hbm, out)
+    if want("ragged"):
+        ragged_rows(fp8, torch, dev, out)
+    if want("prefill_mlp"):
+        prefill_row(fp8, torch, dev, fp8_peak, out)
+    if want("moe"):
+        moe_row(fp8, torch, dev, hbm, fp8_peak, out)
+    torch.cuda.empty_cache()
+    return out
+
+
+def act_quant_row(fp8, torch, dev, hbm, out):
     xa = [syn.normal_bf16_device((4096, 18432), 1.0, 77 + i, dev) for i in range(2)]
     ya = torch.empty((4096, 18432), dtype=torch.float8_e4m3fn, device=dev)
     sa = torch.empty((4096, 144), dtype=torch.float32, device=dev)
@@ -271,7 +288,8 @@ def rows_measurements(fp8, torch, peaks):
                         "frac_hbm": b / ms / 1e6 / hbm}
     del xa, ya, sa, gs
 
-    # weight_dequant 18432 x 7168
+
+def dequant_row(fp8, torch, dev, hbm, out):
     w = syn.normal_bf16_device((18432, 7168), 0.02, 78, dev)
     wq, ws = fp8.fp8_weight_quant(w)
     del w
@@ -283,7 +301,9 @@ def rows_measurements(fp8, torch, peaks):
                              "frac_hbm": b / ms / 1e6 / hbm}
     del wq, ws, yd, g
 
-    # ragged wkv_a 7168 -> 576 with ue8m0 activations, M = 37 and 2049 (48 weight copies > L2)
+
+def ragged_rows(fp8, torch, dev, out):
+    # wkv_a 7168 -> 576 with ue8m0 activations, M = 37 and 2049 (48 weight copies > L2)
     for M in (37, 2049):
         copies = 48 if M == 37 else 8
         wk = [fp8.fp8_weight_quant(syn.normal_bf16_device(syn.WKV_A, 0.02, 900 + i, dev)) for i in range(copies)]
@@ -305,7 +325,9 @@ def rows_measurements(fp8, torch, peaks):
                                      "GB/s": b / ms / 1e6, "TFLOP/s": f / ms / 1e9}
         del wk, g
 
-    # prefill dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2
+
+def prefill_row(fp8, torch, dev, fp8_peak, out):
+    # dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2
     M, D, I = 4096, syn.MLP_DIM, syn.MLP_INTER
     w13q = torch.empty((2 * I, D), dtype=torch.float8_e4m3fn, device=dev)
     w13s = torch.empty((2 * I // 128, D // 128), dtype=torch.float32, device=dev)
@@ -339,7 +361,9 @@ def rows_measurements(fp8, torch, peaks):
     del g13, g2
     del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv, g
 
-    # MoE: 4096 tokens x top-8 of 256 experts (Zipf), w1|w3 [4096, 7168], w2 [7168, 2048] per expert
+
+def moe_row(fp8, torch, dev, hbm, fp8_peak, out):
+    # 4096 tokens x top-8 of 256 experts (Zipf), w1|w3 [4096, 7168], w2 [7168, 2048] per expert
     T, E, K8, D, I = 4096, syn.MOE_EXPERTS, syn.MOE_TOPK, syn.MOE_DIM, syn.MOE_INTER
     rt = syn.moe_routing(T=T, E=E, topk=K8)
     w13q = torch.empty((E, 2 * I, D), dtype=torch.float8_e4m3fn, device=dev)
@@ -382,8 +406,6 @@ def rows_measurements(fp8, torch, peaks):
     out["moe"] = row
     del g13, g2
     del w13q, w2q, g
-    torch.cuda.empty_cache()
-    return out
 
 
 # ------------------------------------------------------------------ reference arm
@@ -444,6 +466,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--only-rows", default="",
+                    help="comma list (act_quant,weight_dequant,ragged,prefill_mlp,moe): run just these "
+                         "rows and print them (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -468,6 +493,10 @@ def main():
     torch.cuda.set_device(local)
     import fp8_block_scaled_07_gb300 as fp8
     peaks, peak_src = load_peaks()
+    if args.only_rows:
+        print(json.dumps({"rows": rows_measurements(fp8, torch, peaks, set(args.only_rows.split(",")))}),
+              flush=True)
+        return
     dec = Decode(fp8, torch)
     M = dec.M
 

@@ -108,13 +108,20 @@ struct Cfg {
     static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
     // small swapped tiles: 5 stages (80 KB of weights in flight) so that two
     // CTAs fit on an SM -- the next launch's CTAs start while this one drains
-    static constexpr int kStages = (kSwap && BN <= 32) ? 5 : (BN >= 128 ? 6 : 8);
+    static constexpr int kStages = (kSwap && BN <= 32) ? 5 : (BN == 256 ? 4 : (BN >= 128 ? 6 : 8));
     static constexpr int kMinBlocks = (kSwap && BN <= 32) ? 2 : 1;
-    static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,32,64,128}
+    // 128x256 tiles: 8 epilogue warps, two per TMEM lane quarter, each owning
+    // 128 of the 256 columns; their warpgroups take registers from warps 0-3
+    static constexpr int kEpiWarps = BN == 256 ? 8 : 4;
+    static constexpr int kThreads = 128 + 32 * kEpiWarps;
+    static constexpr int kCPT = BN * 4 / kEpiWarps;   // accumulator columns per epilogue thread
+    static constexpr bool kSplitRegs = kEpiWarps == 8;
+    static constexpr int kRegsLow = 40, kRegsHigh = 232;   // 40*128 + 232*256 = 168*384
+    static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,...,256}
     static constexpr int kBarBytes = 1024;
     // grouped: per-expert tile prefix; swapped: two chunks of staged scales
     static constexpr int kExtraBytes =
-        V == kGrouped ? (kMaxGroups + 1) * 4 : (kSwap ? 2 * kScaleChunk * BN * 4 : 0);
+        V == kGrouped ? (kMaxGroups + 1 + 16) * 4 : (kSwap ? 2 * kScaleChunk * BN * 4 : 0);
     static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes + kExtraBytes;
     // weight slabs each CTA prefetches into L2 before its inputs are ready
     static constexpr int kL2Prefetch = kStages;
@@ -212,11 +219,11 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
     atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_TIMEOUT));
 }
 
-// Store BN accumulators of one output row (non-swapped layout) or one
-// output column (swapped layout).
-template <int BN, int V>
-__device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int e,
-                                           const float (&acc)[BN]) {
+// Store the CPT accumulators of one output row starting at tile column
+// cofs (non-swapped layout) or of one output column (swapped layout).
+template <int BN, int V, int CPT>
+__device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int e, int cofs,
+                                           const float (&acc)[CPT]) {
     if (V == kDenseSwap) {
         const int n = tg.p_row0 + e;
         if (e >= tg.p_valid) return;
@@ -232,12 +239,13 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
     }
     if (e >= tg.p_valid) return;
     const int64_t row = tg.p_row0 + e;
-    const int col0 = (V == kGrouped) ? tg.q_col0 : tg.q_row0;
+    const int col0 = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) + cofs;
+    const int valid = tg.q_valid - cofs;
     const bool vec = (p.N % 8 == 0);
 #pragma unroll
-    for (int j0 = 0; j0 < BN; j0 += 8) {
+    for (int j0 = 0; j0 < CPT; j0 += 8) {
         const int col = col0 + j0;
-        if (vec && j0 + 8 <= tg.q_valid) {
+        if (vec && j0 + 8 <= valid) {
             if (p.c_bf16) {
                 uint32_t w[4];
 #pragma unroll
@@ -255,11 +263,54 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                if (j0 + i < tg.q_valid) {
+                if (j0 + i < valid) {
                     if (p.c_bf16) p.c_bf16[row * p.N + col + i] = __float2bfloat16_rn(acc[j0 + i]);
                     if (p.c_fp32) p.c_fp32[row * p.N + col + i] = acc[j0 + i];
                 }
             }
+        }
+    }
+}
+
+// Exclusive prefix over experts of their tile counts (m-tiles x tq), by the
+// whole block: each thread takes up to 4 experts, then a block-wide scan.
+// G <= kMaxGroups and NT >= 256, so 4 experts per thread always suffice.
+template <int NT>
+__device__ __forceinline__ void expert_tile_prefix(const int32_t* offsets, int G, int tq, int* s_prefix,
+                                                   int* s_warp) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int per = (G + NT - 1) / NT;
+    const int g0 = t * per;
+    int vals[4];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int g = g0 + i;
+        int v = 0;
+        if (i < per && g < G) {
+            const int cnt = __ldg(offsets + g + 1) - __ldg(offsets + g);
+            v = ((cnt + 127) / 128) * tq;
+        }
+        vals[i] = v;
+        local += v;
+    }
+    int inc = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) s_warp[w] = inc;
+    __syncthreads();
+    int run = inc - local;
+    for (int i = 0; i < w; ++i) run += s_warp[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int g = g0 + i;
+        if (i < per && g < G) {
+            s_prefix[g] = run;
+            run += vals[i];
+            if (g == G - 1) s_prefix[G] = run;
         }
     }
 }
@@ -302,7 +353,7 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const v
 }
 
 template <int BN, int V>
-__global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
+__global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlocks))
     gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
                 const Params p) {
     using C = Cfg<BN, V>;
@@ -328,7 +379,6 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) FP8BS_TRACE(0);
-    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -337,10 +387,10 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 128);
+            mbar_init(&tempty[i], 32 * C::kEpiWarps);
         }
         mbar_init(mma_done, 1);
-        mbar_init(epi_bar, 128);
+        mbar_init(epi_bar, 32 * C::kEpiWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -369,22 +419,14 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
     }
     griddep_wait();   // inputs written by earlier launches are visible from here on
     int num_tiles = p.num_tiles;
-    if (V == kGrouped) {
-        // exclusive prefix over experts of (m-tiles x n-tiles)
-        const int tq = p.N / BN;
-        if (threadIdx.x == 0) {
-            int acc = 0;
-            for (int g = 0; g < p.G; ++g) {
-                s_prefix[g] = acc;
-                const int cnt = p.offsets[g + 1] - p.offsets[g];
-                acc += ((cnt + 127) / 128) * tq;
-            }
-            s_prefix[p.G] = acc;
-        }
-    }
+    if constexpr (V == kGrouped)
+        expert_tile_prefix<C::kThreads>(p.offsets, p.G, p.N / BN, s_prefix, s_prefix + kMaxGroups + 1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // dependents may launch only once this CTA holds its tensor memory: a
+    // dependent CTA on the same SM must never take columns this one needs
+    if (threadIdx.x == 0) griddep_launch_dependents();
     if (V == kGrouped) num_tiles = s_prefix[p.G];
     const uint32_t tmem_base = *tmem_holder;
     if (threadIdx.x == 0) FP8BS_TRACE(1);
@@ -393,6 +435,9 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
     it.init(p, num_tiles);
     Seg sg;
 
+    if (warp < 4) {
+    // whole warpgroups change their register budgets: 0-3 give, 4-11 take
+    if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
@@ -452,15 +497,19 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
             const volatile int never = 0;
             if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
         }
-    } else if (warp >= kEpiWarp0) {
+    }
+    } else {
+        if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
         // ---------------------------------------------------------- epilogue
+        constexpr int CPT = C::kCPT;
         const int q = warp & 3;                     // TMEM lane quarter
         const int e = q * 32 + lane;                // row of the tile (TMEM lane)
+        const int cofs = ((warp - kEpiWarp0) >> 2) * CPT;   // first tile column of this thread
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         uint32_t slab = 0, epi_phase = 0, chunk_ctr = 0;
         bool ok = true;
         // one finished slab: wait for it in TMEM, promote it, free the buffer
-        auto take_slab = [&](float (&acc)[BN], const float* sc_col, float sc) -> bool {
+        auto take_slab = [&](float (&acc)[CPT], const float* sc_col, float sc) -> bool {
             const int buf = slab & 1;
             if (!mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag)) {
                 set_abort(abort_flag);
@@ -468,8 +517,8 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
             }
             tc_fence_after();
             if (slab == 0 && e == 0) FP8BS_TRACE(4);
-            promote<BN, V == kDenseSwap>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN), acc,
-                                         sc_col, sc);
+            promote<CPT, V == kDenseSwap>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs),
+                                          acc, sc_col, sc);
             tc_fence_before();
             mbar_arrive(&tempty[buf]);
             ++slab;
@@ -477,9 +526,9 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
         };
         while (ok && it.next(sg)) {
             const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
-            float acc[BN];
+            float acc[CPT];
 #pragma unroll
-            for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
             if constexpr (V == kDenseSwap) {
                 // scale products b_s[block] * a_s[token] of 32 slabs at a time,
                 // staged in shared memory one chunk ahead
@@ -516,41 +565,48 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
                 }
                 ++chunk_ctr;
             } else {
-                // per-row a_s and per-block b_s, prefetched 8 slabs ahead in registers
+                // per-row a_s and per-block b_s, prefetched PF slabs ahead in registers
                 const float* ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
                 const float* qs = (V == kDense)
-                                      ? p.b_s + static_cast<int64_t>(tg.q_row0 / 128) * p.KB
-                                      : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + tg.q_col0 / 128) * p.KB;
-                float cs[8], na[8], nb[8];
-                auto load8 = [&](int base) {
+                                      ? p.b_s + static_cast<int64_t>((tg.q_row0 + cofs) / 128) * p.KB
+                                      : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + (tg.q_col0 + cofs) / 128) * p.KB;
+                constexpr int PF = CPT >= 128 ? 4 : 8;   // prefetch distance (slabs)
+                float cs[PF], na[PF], nb[PF];
+                auto load_next = [&](int base) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < PF; ++i) {
                         const int kb = base + i;
                         na[i] = kb < sg.k1 ? __ldg(ps + kb) : 0.0f;
                         nb[i] = kb < sg.k1 ? __ldg(qs + kb) : 0.0f;
                     }
                 };
-                load8(sg.k0);
+                load_next(sg.k0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) cs[i] = na[i] * nb[i];
-                load8(sg.k0 + 8);
-                for (int kc = sg.k0; kc < sg.k1 && ok; kc += 8) {
+                for (int i = 0; i < PF; ++i) cs[i] = na[i] * nb[i];
+                load_next(sg.k0 + PF);
+                for (int kc = sg.k0; kc < sg.k1 && ok; kc += PF) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < PF; ++i) {
                         if (ok && kc + i < sg.k1) ok = take_slab(acc, nullptr, cs[i]);
                     }
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) cs[i] = na[i] * nb[i];
-                    load8(kc + 16);
+                    for (int i = 0; i < PF; ++i) cs[i] = na[i] * nb[i];
+                    load_next(kc + 2 * PF);
                 }
             }
             if (!ok) break;
             if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
-                store_tile<BN, V>(p, tg, e, acc);
+                store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
                 continue;
             }
-            // ---- stream-K fixup (dense only): partial tile
+            // ---- stream-K fixup (dense only): partial tile.  The 128x256
+            // kernels only ever run whole tiles (the host plans them so).
+            if constexpr (C::kSplitRegs) {
+                set_abort(abort_flag);
+                ok = false;
+                break;
+            } else {
             const long long U = p.total_units;
             const int P = gridDim.x;
             const long long u_first = static_cast<long long>(sg.tile) * p.KB;
@@ -563,34 +619,34 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
                 return p.partials + (static_cast<int64_t>(c) * 2 + which) * (128 * BN);
             };
             // partial tile layout: [row e][BN columns], 16-byte vectors per thread
-            float* mine = slot_of(blockIdx.x) + e * BN;
+            float* mine = slot_of(blockIdx.x) + e * BN + cofs;
 #pragma unroll
-            for (int j = 0; j < BN; j += 4)
+            for (int j = 0; j < CPT; j += 4)
                 __stcg(reinterpret_cast<float4*>(mine + j), make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
             __threadfence();
             if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
-            if (e == 0) *ticket_box = atomicAdd(p.counters + sg.tile, 1);
+            if (e == 0 && cofs == 0) *ticket_box = atomicAdd(p.counters + sg.tile, 1);
             if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
             const int ticket = *ticket_box;
             if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
             if (ticket == nseg - 1) {
                 __threadfence();
 #pragma unroll
-                for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
+                for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
                 // fixed summation order (segment 0, 1, ...): deterministic; each
                 // batch keeps 8-16 vector loads in flight before adding them
-                constexpr int kFloats = BN <= 32 ? 32 : 64; // floats in flight per thread
-                constexpr int CW = BN < kFloats ? BN : kFloats;   // columns per chunk
-                constexpr int SB = kFloats / CW;                   // segments per batch
+                constexpr int kFloats = CPT <= 32 ? 32 : 64; // floats in flight per thread
+                constexpr int CW = CPT < kFloats ? CPT : kFloats;  // columns per chunk
+                constexpr int SB = kFloats / CW;                    // segments per batch
 #pragma unroll
-                for (int c0 = 0; c0 < BN; c0 += CW) {
+                for (int c0 = 0; c0 < CPT; c0 += CW) {
                     for (int s0 = 0; s0 < nseg; s0 += SB) {
                         float4 v[SB][CW / 4];
 #pragma unroll
                         for (int b = 0; b < SB; ++b) {
                             if (s0 + b < nseg) {
                                 const float4* src = reinterpret_cast<const float4*>(
-                                    slot_of(c_first + s0 + b) + e * BN + c0);
+                                    slot_of(c_first + s0 + b) + e * BN + cofs + c0);
 #pragma unroll
                                 for (int j = 0; j < CW / 4; ++j) v[b][j] = __ldcg(src + j);
                             }
@@ -609,8 +665,9 @@ __global__ void __launch_bounds__(kNumThreads, (Cfg<BN, V>::kMinBlocks))
                         }
                     }
                 }
-                store_tile<BN, V>(p, tg, e, acc);
-                if (e == 0) p.counters[sg.tile] = 0;
+                store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
+                if (e == 0 && cofs == 0) p.counters[sg.tile] = 0;
+            }
             }
             if (e == 0) FP8BS_TRACE(6);
         }
@@ -652,6 +709,8 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
     return r == CUDA_SUCCESS;
 }
 
+bool wide_tiles_ok();
+
 struct Plan {
     int variant;   // kDense / kDenseSwap
     int bn;
@@ -676,6 +735,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
         pl.bn = 128;
         pl.tiles_p = static_cast<int>((M + 127) / 128);
         pl.tiles_q = static_cast<int>((N + 127) / 128);
+        // enough 128x256 tiles for whole-tile scheduling: use the wide tile
+        const long long wide = static_cast<long long>(pl.tiles_p) * ((N + 255) / 256);
+        if (wide >= 4LL * sms && wide <= (1LL << 30) && KB > 1 && wide_tiles_ok()) {
+            pl.bn = 256;
+            pl.tiles_q = static_cast<int>((N + 255) / 256);
+        }
     }
     pl.num_tiles = pl.tiles_p * pl.tiles_q;
     pl.total_units = static_cast<long long>(pl.num_tiles) * KB;
@@ -699,7 +764,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
 template <int BN, int V>
 cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& prm, int grid,
                    cudaStream_t st) {
-    constexpr int smem = Cfg<BN, V>::kSmemBytes;
+    using C = Cfg<BN, V>;
+    constexpr int smem = C::kSmemBytes;
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -709,7 +775,26 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& p
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    return launch_pdl(gemm_kernel<BN, V>, dim3(grid), dim3(kNumThreads), smem, st, mp, mq, prm);
+    return launch_pdl(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, mp, mq, prm);
+}
+
+// The 128x256 kernels move registers between warpgroups with setmaxnreg;
+// that is only safe if the kernel was built with the register count the
+// split assumes (launch total >= the sum of the new per-warpgroup counts).
+template <int V>
+bool split_regs_ok() {
+    using C = Cfg<256, V>;
+    cudaFuncAttributes a{};
+    if (cudaFuncGetAttributes(&a, gemm_kernel<256, V>) != cudaSuccess) return false;
+    return a.numRegs * C::kThreads >= C::kRegsLow * 128 + C::kRegsHigh * 32 * C::kEpiWarps;
+}
+
+bool wide_tiles_ok() {
+    static int cache[64] = {0};   // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return false;
+    if (cache[dev] == 0) cache[dev] = (split_regs_ok<kDense>() && split_regs_ok<kGrouped>()) ? 1 : 2;
+    return cache[dev] == 1;
 }
 
 }  // namespace
@@ -789,7 +874,8 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (!swap) {
-        e = launch<128, kDense>(mp, mq, prm, pl.grid, st);
+        e = pl.bn == 256 ? launch<256, kDense>(mp, mq, prm, pl.grid, st)
+                         : launch<128, kDense>(mp, mq, prm, pl.grid, st);
     } else if (pl.bn == 16) {
         e = launch<16, kDenseSwap>(mp, mq, prm, pl.grid, st);
     } else if (pl.bn == 32) {
@@ -826,11 +912,14 @@ extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const vo
     prm.NB = static_cast<int>(N / 128);
     prm.G = G;
     prm.stream_k = 0;
+    const bool wide = (N % 256 == 0) && wide_tiles_ok();
     CUtensorMap mp, mq;
-    if (!make_map(&mp, a, R_max, K, 128) || !make_map(&mq, b, static_cast<int64_t>(G) * N, K, 128))
+    if (!make_map(&mp, a, R_max, K, 128) ||
+        !make_map(&mq, b, static_cast<int64_t>(G) * N, K, wide ? 256 : 128))
         return FP8_ERR_CUDA;
-    cudaError_t e = launch<128, kGrouped>(mp, mq, prm, device_sm_count(),
-                                          static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = wide ? launch<256, kGrouped>(mp, mq, prm, device_sm_count(), st)
+                         : launch<128, kGrouped>(mp, mq, prm, device_sm_count(), st);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

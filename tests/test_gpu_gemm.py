@@ -87,6 +87,17 @@ def test_data_parallel_schedule(fp8):
     _run(fp8, a, as_, b, bs, rows=rows, what="data-parallel")
 
 
+def test_wide_tile_schedule_ragged(fp8):
+    # enough 128x256 tiles for whole-tile scheduling, ragged in M and N
+    M, N, K = 4100, 4736, 256
+    a = syn.random_e4m3_codes((M, K), 31)
+    b = syn.random_e4m3_codes((N, K), 32)
+    as_ = syn.random_scales((M, K // 128), 33)
+    bs = syn.random_scales(((N + 127) // 128, K // 128), 34)
+    rows = np.r_[0:2, 127:129, 2047, 4095:4100]
+    _run(fp8, a, as_, b, bs, rows=rows, what="wide tiles")
+
+
 def test_prefill_mlp_shapes_sampled(fp8):
     x = syn.mlp_activations(M=4096)
     aq, as_ = oracle.act_quant(x)
