@@ -292,7 +292,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
+#ifdef FP8BS_NO_PDL   // profiling builds only: plain stream order
+    cfg.numAttrs = 0;
+#else
     cfg.numAttrs = 1;
+#endif
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -818,6 +818,10 @@ int gemm_read_and_clear_status(cudaStream_t st) {
 using namespace fp8bs;
 
 #ifdef FP8BS_TRACE_ENABLED
+extern "C" int fp8_debug_clear_trace(void) {
+    static unsigned long long zero[1024][8];
+    return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
+}
 extern "C" int fp8_debug_read_trace(unsigned long long* host, int n_ctas) {
     if (n_ctas > 1024) n_ctas = 1024;
     return cudaMemcpyFromSymbol(host, g_trace, static_cast<size_t>(n_ctas) * 8 * 8) == cudaSuccess ? 0 : 1;
