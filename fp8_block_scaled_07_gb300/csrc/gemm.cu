@@ -41,13 +41,13 @@ __device__ int g_gemm_status;   // FP8_OK or FP8_ERR_TIMEOUT, read by fp8_device
 // Optional per-CTA timeline (global timer, ns) for profiling builds only;
 // compiles to nothing unless FP8BS_TRACE_ENABLED is defined.
 #ifdef FP8BS_TRACE_ENABLED
-__device__ unsigned long long g_trace[1024][8];
+__device__ unsigned long long g_trace[4][512][12];
 #define FP8BS_TRACE(slot)                                                            \
     do {                                                                             \
-        if (blockIdx.x < 1024) {                                                     \
+        if (blockIdx.x < 512) {                                                      \
             unsigned long long t_;                                                   \
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                    \
-            g_trace[blockIdx.x][slot] = t_;                                          \
+            g_trace[p.trace_slot & 3][blockIdx.x][slot] = t_;                        \
         }                                                                            \
     } while (0)
 #else
@@ -88,6 +88,8 @@ struct Params {
     int num_tiles;             // dense
     int stream_k;              // 1: stream-K schedule over total_units
     long long total_units;     // num_tiles * KB
+    int trace_slot;            // profiling builds: which timeline buffer this launch fills
+    int ksplit;                // >0: cluster split-K, CTA = (tile, K part), cluster of ksplit CTAs
 };
 
 struct Tile {
@@ -147,7 +149,12 @@ struct SegIter {
         KB = p.KB;
         sk = p.stream_k != 0;
         num_tiles = ntiles;
-        if (sk) {
+        if (p.ksplit > 0) {   // one segment: K part (blockIdx % c) of tile (blockIdx / c)
+            const int c = p.ksplit, t0 = blockIdx.x / c, part = blockIdx.x % c;
+            sk = true;
+            u = static_cast<long long>(t0) * KB + static_cast<long long>(part) * KB / c;
+            hi = static_cast<long long>(t0) * KB + static_cast<long long>(part + 1) * KB / c;
+        } else if (sk) {
             u = sk_start(blockIdx.x, p.total_units, gridDim.x);
             hi = sk_start(blockIdx.x + 1, p.total_units, gridDim.x);
         } else {
@@ -370,7 +377,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     uint64_t* tempty = bars + 2 * S + 2;   // 2
     uint64_t* mma_done = bars + 2 * S + 4; // 1
     uint64_t* epi_bar = bars + 2 * S + 5;  // epilogue-group barrier
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+    uint64_t* red_bar = bars + 2 * S + 6;  // cluster split-K: all partials of the tile ready
+    uint64_t* done_bar = bars + 2 * S + 7; // cluster split-K: every CTA done reading partials
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
     int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kBarBytes);
@@ -391,6 +400,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         }
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
+        mbar_init(red_bar, p.ksplit > 1 ? p.ksplit : 1);
+        mbar_init(done_bar, p.ksplit > 1 ? p.ksplit : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -418,12 +429,16 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         tmem_relinquish();
     }
     griddep_wait();   // inputs written by earlier launches are visible from here on
+    if (threadIdx.x == 0) FP8BS_TRACE(8);
     int num_tiles = p.num_tiles;
     if constexpr (V == kGrouped)
         expert_tile_prefix<C::kThreads>(p.offsets, p.G, p.N / BN, s_prefix, s_prefix + kMaxGroups + 1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // every CTA of a split-K cluster has initialised its barriers before any
+    // of them may arrive on a remote one
+    if (p.ksplit > 1) cluster_sync_all();
     // dependents may launch only once this CTA holds its tensor memory: a
     // dependent CTA on the same SM must never take columns this one needs
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -600,6 +615,65 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
                 continue;
             }
+            if constexpr (V == kDenseSwap) {
+                if (p.ksplit > 1) {
+                    // ---- cluster split-K: partials meet in shared memory
+                    const int c = p.ksplit;
+                    const uint32_t rank = cluster_rank();
+                    float* part = reinterpret_cast<float*>(sP);   // pipeline stages are idle now
+#pragma unroll
+                    for (int j = 0; j < BN; j += 4)
+                        *reinterpret_cast<float4*>(part + e * BN + j) =
+                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    fence_acq_rel_cluster();
+                    if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
+                    if (e == 0)
+                        for (int r = 0; r < c; ++r) mbar_arrive_remote(cluster_map(smem_u32(red_bar), r));
+                    if (!mbar_wait(red_bar, 0, abort_flag)) {
+                        set_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    // rank r reduces tile rows [r*128/c, (r+1)*128/c) over all partials,
+                    // in rank order (deterministic); consecutive threads take
+                    // consecutive rows (= output columns) of one token group
+                    const int rows = 128 / c, groups = BN / 4;
+                    const uint32_t part_s = smem_u32(part);
+                    for (int idx = e; idx < rows * groups; idx += 128) {
+                        const int row = static_cast<int>(rank) * rows + idx % rows;
+                        const int g4 = idx / rows;
+                        const uint32_t off = static_cast<uint32_t>((row * BN + g4 * 4) * 4);
+                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int r = 0; r < c; ++r) {
+                            const float4 v = ld_cluster_f4(cluster_map(part_s + off, r));
+                            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                        }
+                        const int n = tg.p_row0 + row;
+                        if (row < tg.p_valid) {
+                            const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int j = g4 * 4 + i;
+                                if (j < tg.q_valid) {
+                                    const int64_t o = static_cast<int64_t>(tg.q_row0 + j) * p.N + n;
+                                    if (p.c_bf16) p.c_bf16[o] = __float2bfloat16_rn(vals[i]);
+                                    if (p.c_fp32) p.c_fp32[o] = vals[i];
+                                }
+                            }
+                        }
+                    }
+                    // no CTA may leave while another still reads its partial
+                    if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
+                    if (e == 0)
+                        for (int r = 0; r < c; ++r) mbar_arrive_remote(cluster_map(smem_u32(done_bar), r));
+                    if (!mbar_wait(done_bar, 0, abort_flag)) {
+                        set_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    continue;
+                }
+            }
             // ---- stream-K fixup (dense only): partial tile.  The 128x256
             // kernels only ever run whole tiles (the host plans them so).
             if constexpr (C::kSplitRegs) {
@@ -625,8 +699,10 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 __stcg(reinterpret_cast<float4*>(mine + j), make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
             __threadfence();
             if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
+            if (e == 0) FP8BS_TRACE(9);
             if (e == 0 && cofs == 0) *ticket_box = atomicAdd(p.counters + sg.tile, 1);
             if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
+            if (e == 0) FP8BS_TRACE(10);
             const int ticket = *ticket_box;
             if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
             if (ticket == nseg - 1) {
@@ -720,6 +796,7 @@ struct Plan {
     long long total_units;
     size_t ws_bytes;   // counters + partial slots
     size_t counters_bytes;
+    int ksplit;        // swapped layout: CTAs (one cluster) per output tile, 0 = not used
 };
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
@@ -744,6 +821,20 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
     }
     pl.num_tiles = pl.tiles_p * pl.tiles_q;
     pl.total_units = static_cast<long long>(pl.num_tiles) * KB;
+    const long long slots = static_cast<long long>(sms) * (pl.bn <= 32 ? 2 : 1);
+    if (pl.variant == kDenseSwap && pl.num_tiles <= slots) {
+        // decode: every output tile gets a cluster of c CTAs splitting K (at
+        // least 4 slabs each); c is the largest of 1, 2, 4, 8 that keeps all
+        // CTAs resident at once (two per SM for the small tiles).  With more
+        // tiles than resident CTAs, stream-K below balances the work instead.
+        int c = 1;
+        while (c < 8 && static_cast<long long>(pl.num_tiles) * c * 2 <= slots && KB / (c * 2) >= 4) c *= 2;
+        pl.ksplit = c;
+        pl.stream_k = 0;
+        pl.grid = pl.num_tiles * c;
+        pl.ws_bytes = 0;
+        return pl;
+    }
     if (pl.num_tiles >= 4 * sms || pl.num_tiles > kMaxSkTiles || KB == 1) {
         pl.stream_k = 0;
         pl.grid = std::min(pl.num_tiles, sms);
@@ -763,7 +854,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
 
 template <int BN, int V>
 cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& prm, int grid,
-                   cudaStream_t st) {
+                   cudaStream_t st, unsigned cluster = 1) {
     using C = Cfg<BN, V>;
     constexpr int smem = C::kSmemBytes;
     static int configured[64] = {0};
@@ -775,7 +866,8 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& p
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    return launch_pdl(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, mp, mq, prm);
+    return launch_pdl_cluster(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, cluster, mp, mq,
+                              prm);
 }
 
 // The 128x256 kernels move registers between warpgroups with setmaxnreg;
@@ -818,13 +910,14 @@ int gemm_read_and_clear_status(cudaStream_t st) {
 using namespace fp8bs;
 
 #ifdef FP8BS_TRACE_ENABLED
+static int g_trace_next = 0;
 extern "C" int fp8_debug_clear_trace(void) {
-    static unsigned long long zero[1024][8];
+    static unsigned long long zero[4][512][12];
+    g_trace_next = 0;
     return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
-extern "C" int fp8_debug_read_trace(unsigned long long* host, int n_ctas) {
-    if (n_ctas > 1024) n_ctas = 1024;
-    return cudaMemcpyFromSymbol(host, g_trace, static_cast<size_t>(n_ctas) * 8 * 8) == cudaSuccess ? 0 : 1;
+extern "C" int fp8_debug_read_trace(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * 4 * 512 * 12) == cudaSuccess ? 0 : 1;
 }
 #endif
 
@@ -865,6 +958,10 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     prm.num_tiles = pl.num_tiles;
     prm.stream_k = pl.stream_k;
     prm.total_units = pl.total_units;
+    prm.ksplit = pl.ksplit;
+#ifdef FP8BS_TRACE_ENABLED
+    prm.trace_slot = g_trace_next++ & 3;
+#endif
     if (pl.ws_bytes > 0) {
         prm.counters = static_cast<int*>(workspace);
         prm.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
@@ -881,11 +978,11 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
         e = pl.bn == 256 ? launch<256, kDense>(mp, mq, prm, pl.grid, st)
                          : launch<128, kDense>(mp, mq, prm, pl.grid, st);
     } else if (pl.bn == 16) {
-        e = launch<16, kDenseSwap>(mp, mq, prm, pl.grid, st);
+        e = launch<16, kDenseSwap>(mp, mq, prm, pl.grid, st, pl.ksplit);
     } else if (pl.bn == 32) {
-        e = launch<32, kDenseSwap>(mp, mq, prm, pl.grid, st);
+        e = launch<32, kDenseSwap>(mp, mq, prm, pl.grid, st, pl.ksplit);
     } else {
-        e = launch<64, kDenseSwap>(mp, mq, prm, pl.grid, st);
+        e = launch<64, kDenseSwap>(mp, mq, prm, pl.grid, st, pl.ksplit);
     }
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }

@@ -108,23 +108,46 @@ def test_prefill_mlp_shapes_sampled(fp8):
     _run(fp8, aq, as_, bq, bs, rows=rows, what="w1 M=4096")
 
 
+def _random_case(M, N, K, seed):
+    a = syn.random_e4m3_codes((M, K), seed)
+    b = syn.random_e4m3_codes((N, K), seed + 1)
+    as_ = syn.random_scales((M, K // 128), seed + 2)
+    bs = syn.random_scales(((N + 127) // 128, K // 128), seed + 3)
+    return a, as_, b, bs
+
+
 def test_workspace_too_small_is_reported(fp8):
-    lin = syn.decode_linears(16, layers=["wq_a"])[0]
-    aq, as_, bq, bs = _quantised(lin)
-    need = fp8.fp8_gemm_workspace_size(16, 1536, 7168)
+    # few output tiles: K split across CTAs with partials in the workspace
+    M, N, K = 300, 384, 1024
+    need = fp8.fp8_gemm_workspace_size(M, N, K)
     assert need > 0
+    a, as_, b, bs = _random_case(M, N, K, 50)
     ws = torch.zeros(need // 2, dtype=torch.uint8, device="cuda")
     with pytest.raises(fp8.Fp8Error) as ei:
-        fp8.fp8_gemm(dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs), workspace=ws)
+        fp8.fp8_gemm(dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs), workspace=ws)
     assert ei.value.status == 5
 
 
+def test_decode_shapes_need_no_workspace(fp8):
+    for N, K in syn.DECODE_LAYERS.values():
+        assert fp8.fp8_gemm_workspace_size(16, N, K) == 0
+
+
+@pytest.mark.parametrize("layer", ["wq_a", "wo"])
+def test_cluster_split_is_deterministic(fp8, layer):
+    lin = syn.decode_linears(16, layers=[layer])[0]
+    args = tuple(f(v) for f, v in zip((dev_e4m3, dev_f32, dev_e4m3, dev_f32), _quantised(lin)))
+    outs = [host_f32(fp8.fp8_gemm(*args, out_bf16=False, out_fp32=True)[1]) for _ in range(3)]
+    fp8.fp8_device_status()
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
 def test_repeat_calls_are_deterministic_and_leave_workspace_clean(fp8):
-    lin = syn.decode_linears(16, layers=["wo"])[0]
-    aq, as_, bq, bs = _quantised(lin)
-    need = fp8.fp8_gemm_workspace_size(16, 7168, 16384)
+    M, N, K = 300, 384, 1024
+    a, as_, b, bs = _random_case(M, N, K, 60)
+    need = fp8.fp8_gemm_workspace_size(M, N, K)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    args = (dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs))
+    args = (dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs))
     outs = [host_f32(fp8.fp8_gemm(*args, out_bf16=False, out_fp32=True, workspace=ws)[1]) for _ in range(3)]
     fp8.fp8_device_status()
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
@@ -136,12 +159,16 @@ def test_repeat_calls_are_deterministic_and_leave_workspace_clean(fp8):
 def test_one_workspace_serves_shapes_in_any_order(fp8):
     # a call with few split tiles leaves partials where a later call with
     # more split tiles keeps counters: counters must live apart from partials
-    ws = torch.zeros(fp8.fp8_gemm_workspace_size(16, 24576, 16384), dtype=torch.uint8, device="cuda")
-    for M, name in [(16, "wq_a"), (16, "wo"), (16, "wq_b"), (1, "wq_b"), (16, "wq_a")]:
-        lin = syn.decode_linears(M, layers=[name])[0]
-        aq, as_, bq, bs = _quantised(lin)
-        assert fp8.fp8_gemm_workspace_size(M, *lin.w.shape) <= ws.numel()
-        cb, cf = fp8.fp8_gemm(dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs), out_fp32=True, workspace=ws)
+    shapes = [(129, 136, 256), (64, 24576, 1536), (300, 384, 1024), (64, 24576, 1536), (129, 136, 256)]
+    ws = torch.zeros(max(fp8.fp8_gemm_workspace_size(*sh) for sh in shapes), dtype=torch.uint8, device="cuda")
+    for i, (M, N, K) in enumerate(shapes):
+        assert fp8.fp8_gemm_workspace_size(M, N, K) > 0
+        a, as_, b, bs = _random_case(M, N, K, 70 + i)
+        cb, cf = fp8.fp8_gemm(dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs), out_fp32=True, workspace=ws)
         fp8.fp8_device_status()
-        ref, mag = oracle.gemm(aq, as_, bq, bs)
-        check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"{name} M={M} shared workspace")
+        rows = None if M * N <= 1 << 20 else np.r_[0:3, M - 3:M]
+        ref, mag = oracle.gemm(a, as_, b, bs, rows=rows)
+        cf_h, cb_h = host_f32(cf), host_bits(cb)
+        if rows is not None:
+            cf_h, cb_h = cf_h[rows], cb_h[rows]
+        check_gemm(ref, mag, cf_h, cb_h, f"{M}x{N}x{K} shared workspace")

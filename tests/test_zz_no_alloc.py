@@ -43,28 +43,31 @@ def _noalloc(fp8, a, a_s, b, b_s, M, N, K):
     return st, cb, cf
 
 
-def _case(name, M):
-    lin = syn.decode_linears(M, layers=[name])[0]
-    aq, as_ = oracle.act_quant(lin.x)
-    bq, bs = oracle.weight_quant(lin.w)
+def _case(M, N, K, seed):
+    aq = syn.random_e4m3_codes((M, K), seed)
+    bq = syn.random_e4m3_codes((N, K), seed + 1)
+    as_ = syn.random_scales((M, K // 128), seed + 2)
+    bs = syn.random_scales(((N + 127) // 128, K // 128), seed + 3)
     return aq, as_, bq, bs
 
 
 def test_two_calls_in_a_row_match_the_workspace_entry_point(fp8):
-    cases = [("wo", 16), ("wq_a", 16)]          # both split K across CTAs (use scratch)
+    # two shapes with few output tiles: K is split across CTAs with partial
+    # tiles in the scratch (the second call finds the first one's leftovers)
+    cases = [(300, 384, 1024), (129, 136, 256)]
     results = []
-    for name, M in cases:
-        aq, as_, bq, bs = _case(name, M)
-        N, K = syn.DECODE_LAYERS[name]
+    for i, (M, N, K) in enumerate(cases):
+        name = f"{M}x{N}x{K}"
+        aq, as_, bq, bs = _case(M, N, K, 40 + 10 * i)
         assert 0 < fp8.fp8_gemm_workspace_size(M, N, K) <= SCRATCH_BYTES
         args = (dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs))
         st, cb, cf = _noalloc(fp8, *args, M, N, K)
         assert st == 0, fp8.lib.fp8_status_string(st)
-        results.append((name, M, aq, as_, bq, bs, args, cb, cf))
+        results.append((name, aq, as_, bq, bs, args, cb, cf))
     fp8.fp8_device_status()
-    for name, M, aq, as_, bq, bs, args, cb, cf in results:
+    for name, aq, as_, bq, bs, args, cb, cf in results:
         ref, mag = oracle.gemm(aq, as_, bq, bs)
-        check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"noalloc {name} M={M}")
+        check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"noalloc {name}")
         wb, wf = fp8.fp8_gemm(*args, out_bf16=True, out_fp32=True)
         fp8.fp8_device_status()
         diff = np.abs(host_f32(cf).astype(np.float64) - host_f32(wf))
@@ -72,8 +75,8 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(fp8):
 
 
 def test_shapes_needing_more_scratch_are_rejected(fp8):
-    # 64 tokens x 20 output tiles: split-K partials of ~10 MB on 152 SMs
-    M, N, K = 64, 2560, 7168
+    # 64 tokens x 192 output tiles: stream-K partials of ~10 MB on 152 SMs
+    M, N, K = 64, 24576, 1536
     if fp8.fp8_gemm_workspace_size(M, N, K) <= SCRATCH_BYTES:
         pytest.skip("this device's schedule fits the fixed scratch")
     a = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
