@@ -291,6 +291,12 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t remote_saddr) {
     return v;
 }
 
+__device__ __forceinline__ void st_cluster_f4(uint32_t remote_saddr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote_saddr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

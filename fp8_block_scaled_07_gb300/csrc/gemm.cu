@@ -110,7 +110,7 @@ struct Cfg {
     static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
     // small swapped tiles: 5 stages (80 KB of weights in flight) so that two
     // CTAs fit on an SM -- the next launch's CTAs start while this one drains
-    static constexpr int kStages = (kSwap && BN <= 32) ? 5 : (BN == 256 ? 4 : (BN >= 128 ? 6 : 8));
+    static constexpr int kStages = (kSwap && BN <= 32) ? 5 : (BN == 256 ? 4 : (BN >= 128 ? 6 : 7));
     static constexpr int kMinBlocks = (kSwap && BN <= 32) ? 2 : 1;
     // 128x256 tiles: 8 epilogue warps, two per TMEM lane quarter, each owning
     // 128 of the 256 columns; their warpgroups take registers from warps 0-3
@@ -122,8 +122,10 @@ struct Cfg {
     static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,...,256}
     static constexpr int kBarBytes = 1024;
     // grouped: per-expert tile prefix; swapped: two chunks of staged scales
+    // swapped: staged scales + the split-K receive buffer (128 x BN fp32)
+    static constexpr int kRecvBytes = kSwap ? 128 * BN * 4 : 0;
     static constexpr int kExtraBytes =
-        V == kGrouped ? (kMaxGroups + 1 + 16) * 4 : (kSwap ? 2 * kScaleChunk * BN * 4 : 0);
+        V == kGrouped ? (kMaxGroups + 1 + 16) * 4 : (kSwap ? 2 * kScaleChunk * BN * 4 + kRecvBytes : 0);
     static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes + kExtraBytes;
     // weight slabs each CTA prefetches into L2 before its inputs are ready
     static constexpr int kL2Prefetch = kStages;
@@ -144,16 +146,19 @@ struct SegIter {
     // data-parallel: tiles blockIdx.x + i * gridDim.x; stream-K: units [lo, hi)
     long long u, hi;
     int t, stride, num_tiles, KB;
-    bool sk;
+    int cl_tile, cl_k0, cl_k1;
+    bool sk, cl = false, cl_done = false;
     __device__ void init(const Params& p, int ntiles) {
         KB = p.KB;
         sk = p.stream_k != 0;
         num_tiles = ntiles;
         if (p.ksplit > 0) {   // one segment: K part (blockIdx % c) of tile (blockIdx / c)
-            const int c = p.ksplit, t0 = blockIdx.x / c, part = blockIdx.x % c;
-            sk = true;
-            u = static_cast<long long>(t0) * KB + static_cast<long long>(part) * KB / c;
-            hi = static_cast<long long>(t0) * KB + static_cast<long long>(part + 1) * KB / c;
+            const unsigned c = static_cast<unsigned>(p.ksplit), b = blockIdx.x;
+            const unsigned t0 = b / c, part = b - t0 * c, kb = static_cast<unsigned>(KB);
+            cl_tile = static_cast<int>(t0);
+            cl_k0 = static_cast<int>(part * kb / c);
+            cl_k1 = static_cast<int>((part + 1) * kb / c);
+            cl = true;
         } else if (sk) {
             u = sk_start(blockIdx.x, p.total_units, gridDim.x);
             hi = sk_start(blockIdx.x + 1, p.total_units, gridDim.x);
@@ -163,6 +168,14 @@ struct SegIter {
         }
     }
     __device__ bool next(Seg& s) {
+        if (cl) {
+            if (cl_done) return false;
+            s.tile = cl_tile;
+            s.k0 = cl_k0;
+            s.k1 = cl_k1;
+            cl_done = true;
+            return true;
+        }
         if (sk) {
             if (u >= hi) return false;
             s.tile = static_cast<int>(u / KB);
@@ -377,13 +390,13 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     uint64_t* tempty = bars + 2 * S + 2;   // 2
     uint64_t* mma_done = bars + 2 * S + 4; // 1
     uint64_t* epi_bar = bars + 2 * S + 5;  // epilogue-group barrier
-    uint64_t* red_bar = bars + 2 * S + 6;  // cluster split-K: all partials of the tile ready
-    uint64_t* done_bar = bars + 2 * S + 7; // cluster split-K: every CTA done reading partials
+    uint64_t* red_bar = bars + 2 * S + 6;  // cluster split-K: all partials pushed to this CTA
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
     int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kBarBytes);
     float* s_scale = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kBarBytes);
+    float* s_recv = s_scale + 2 * kScaleChunk * BN;   // swapped: split-K partials pushed here
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -401,7 +414,6 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
         mbar_init(red_bar, p.ksplit > 1 ? p.ksplit : 1);
-        mbar_init(done_bar, p.ksplit > 1 ? p.ksplit : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -428,22 +440,26 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         tmem_alloc(tmem_holder, C::kTmemCols);
         tmem_relinquish();
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    // every CTA of a split-K cluster has initialised its barriers before any
+    // of them may arrive on a remote one
+    if (p.ksplit > 1) cluster_sync_all();
+    // dependents may launch only once this CTA holds its tensor memory (a
+    // dependent CTA on the same SM must never take columns this one needs);
+    // an otherwise idle warp signals, so the producer is not delayed
+    if (threadIdx.x == 96) griddep_launch_dependents();
     griddep_wait();   // inputs written by earlier launches are visible from here on
     if (threadIdx.x == 0) FP8BS_TRACE(8);
     int num_tiles = p.num_tiles;
     if constexpr (V == kGrouped)
         expert_tile_prefix<C::kThreads>(p.offsets, p.G, p.N / BN, s_prefix, s_prefix + kMaxGroups + 1);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // every CTA of a split-K cluster has initialised its barriers before any
-    // of them may arrive on a remote one
-    if (p.ksplit > 1) cluster_sync_all();
-    // dependents may launch only once this CTA holds its tensor memory: a
-    // dependent CTA on the same SM must never take columns this one needs
-    if (threadIdx.x == 0) griddep_launch_dependents();
-    if (V == kGrouped) num_tiles = s_prefix[p.G];
-    const uint32_t tmem_base = *tmem_holder;
+    if constexpr (V == kGrouped) {
+        __syncthreads();
+        num_tiles = s_prefix[p.G];
+    }
     if (threadIdx.x == 0) FP8BS_TRACE(1);
 
     SegIter it;
@@ -617,37 +633,40 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             }
             if constexpr (V == kDenseSwap) {
                 if (p.ksplit > 1) {
-                    // ---- cluster split-K: partials meet in shared memory
-                    const int c = p.ksplit;
+                    // ---- cluster split-K: every CTA pushes each tile row of its
+                    // partial to the CTA that owns that row (rank = row / rows);
+                    // the owner reduces the c partials in rank order
+                    const int c = p.ksplit, rows = 128 / c;
                     const uint32_t rank = cluster_rank();
-                    float* part = reinterpret_cast<float*>(sP);   // pipeline stages are idle now
+                    {
+                        const uint32_t owner = static_cast<uint32_t>(e / rows);
+                        const uint32_t dst = cluster_map(
+                            smem_u32(s_recv + (static_cast<int>(rank) * rows + e % rows) * BN), owner);
 #pragma unroll
-                    for (int j = 0; j < BN; j += 4)
-                        *reinterpret_cast<float4*>(part + e * BN + j) =
-                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                    fence_acq_rel_cluster();
+                        for (int j = 0; j < BN; j += 4)
+                            st_cluster_f4(dst + j * 4, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
+                    }
                     if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
-                    if (e == 0)
-                        for (int r = 0; r < c; ++r) mbar_arrive_remote(cluster_map(smem_u32(red_bar), r));
+                    // lane r of the first epilogue warp tells owner r; each release covers
+                    // the pushes of every thread ordered before it by the barrier above
+                    if (e < c) mbar_arrive_remote(cluster_map(smem_u32(red_bar), static_cast<uint32_t>(e)));
                     if (!mbar_wait(red_bar, 0, abort_flag)) {
                         set_abort(abort_flag);
                         ok = false;
                         break;
                     }
-                    // rank r reduces tile rows [r*128/c, (r+1)*128/c) over all partials,
-                    // in rank order (deterministic); consecutive threads take
-                    // consecutive rows (= output columns) of one token group
-                    const int rows = 128 / c, groups = BN / 4;
-                    const uint32_t part_s = smem_u32(part);
+                    if (e == 0) FP8BS_TRACE(10);
+                    // reduce rows [rank*rows, (rank+1)*rows): s_recv[src][row][BN];
+                    // consecutive threads take consecutive rows (= output columns)
+                    const int groups = BN / 4;
                     for (int idx = e; idx < rows * groups; idx += 128) {
-                        const int row = static_cast<int>(rank) * rows + idx % rows;
-                        const int g4 = idx / rows;
-                        const uint32_t off = static_cast<uint32_t>((row * BN + g4 * 4) * 4);
+                        const int lr = idx % rows, g4 = idx / rows;
                         float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
                         for (int r = 0; r < c; ++r) {
-                            const float4 v = ld_cluster_f4(cluster_map(part_s + off, r));
+                            const float4 v = *reinterpret_cast<const float4*>(s_recv + (r * rows + lr) * BN + g4 * 4);
                             sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                         }
+                        const int row = static_cast<int>(rank) * rows + lr;
                         const int n = tg.p_row0 + row;
                         if (row < tg.p_valid) {
                             const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
@@ -662,15 +681,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                             }
                         }
                     }
-                    // no CTA may leave while another still reads its partial
-                    if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
-                    if (e == 0)
-                        for (int r = 0; r < c; ++r) mbar_arrive_remote(cluster_map(smem_u32(done_bar), r));
-                    if (!mbar_wait(done_bar, 0, abort_flag)) {
-                        set_abort(abort_flag);
-                        ok = false;
-                        break;
-                    }
+                    if (e == 0) FP8BS_TRACE(9);
                     continue;
                 }
             }
