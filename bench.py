@@ -4,19 +4,20 @@ Workload of the headline line: DeepSeek-V3 decode-shaped linears at batch
 M=16 tokens -- wq_a (7168->1536), wq_b (1536->24576), wo (16384->7168) --
 with bf16 activations ~N(0,1) (0.5% outliers x30) and e4m3 weights with
 128x128 fp32 block scales drawn from N(0, 0.02).  One step = act_quant +
-fp8_gemm for each of the three layers (6 kernel launches), replayed from CUDA
-graphs.  Four weight sets (4 x 167 MB) rotate between steps so every step
+fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer
+(the quantisation runs inside the GEMM kernel at this batch), replayed from
+CUDA graphs.  Four weight sets (4 x 167 MB) rotate between steps so every step
 streams its weights from HBM (inputs larger than L2).
 
 value  = algorithmic HBM bytes of the step / device time (GB/s); the
-         algorithmic bytes are what the method must move (weights + their
-         scales, activations in, codes/scales out and back in, outputs);
+         algorithmic bytes are what the method must move at least: e4m3
+         weights + block scales, bf16 activations in, bf16 outputs out;
 e2e    = same metric through the Python binding with host buffers: each
-         step copies the activations host->device, runs the six calls and
-         copies the outputs device->host;
-roofline = the fp8_gemm kernel alone (the dominant kernel): per-launch
-         CUDA-event durations of graphs that replay only that layer's GEMM
-         (four weight rotations), taken right after the timed region;
+         step copies the activations host->device, runs the three calls
+         and copies the outputs device->host;
+roofline = the fused linear kernel (the only kernel of the step): per-launch
+         CUDA-event durations of graphs that replay only that layer's
+         launches (four weight rotations), taken right after the timed region;
 cpu_baseline = the CPU oracle on the host cores over a bounded sample.
 
 With --impl reference the CPU oracle itself is timed on the same workload
@@ -61,8 +62,15 @@ def gemm_flops(M, N, K):
     return 2 * M * N * K
 
 
+def linear_bytes(M, N, K):
+    """What one FP8 linear must move at least: e4m3 weight + block scales,
+    bf16 activations in, bf16 outputs out (quantised activations stay on chip)."""
+    nb, kb = (N + 127) // 128, K // 128
+    return N * K + 4 * nb * kb + 2 * M * K + 2 * M * N
+
+
 def decode_step_bytes(M):
-    return sum(act_quant_bytes(M, K) + gemm_bytes(M, N, K) for N, K in syn.DECODE_LAYERS.values())
+    return sum(linear_bytes(M, N, K) for N, K in syn.DECODE_LAYERS.values())
 
 
 def decode_step_flops(M):
@@ -183,7 +191,7 @@ class Decode:
             self.xq[name] = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
             self.xs[name] = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
             self.y[name] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        need = max(fp8.fp8_gemm_workspace_size(M, *syn.DECODE_LAYERS[n]) for n in LAYERS)
+        need = max(int(fp8.lib.fp8_linear_workspace_size(M, *syn.DECODE_LAYERS[n])) for n in LAYERS)
         self.ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
@@ -192,8 +200,7 @@ class Decode:
         xs = self.x[r] if x is None else x
         for name in LAYERS:
             wq, wsc = self.w[r][name]
-            fp8.fp8_act_quant(xs[name], y=self.xq[name], s=self.xs[name])
-            fp8.fp8_gemm(self.xq[name], self.xs[name], wq, wsc, c_bf16=self.y[name], workspace=self.ws)
+            fp8.fp8_linear(xs[name], wq, wsc, c_bf16=self.y[name], workspace=self.ws)
 
 
 def capture(torch, fn):
@@ -528,8 +535,8 @@ def main():
     ms = t_start.elapsed_time(t_end)
     fp8.fp8_device_status()
 
-    # per-launch fp8_gemm durations: per layer, a graph of its GEMM over the
-    # four weight rotations (inputs already quantised), events around replays
+    # per-launch durations of the fused linear kernel: per layer, a graph of
+    # its launches over the four weight rotations, events around replays
     gemm_ms, gemm_b, per_layer = 0.0, 0, {}
     for name in LAYERS:
         N, K = syn.DECODE_LAYERS[name]
@@ -537,12 +544,12 @@ def main():
         def gemms(name=name):
             for r in range(dec.R):
                 wq, wsc = dec.w[r][name]
-                fp8.fp8_gemm(dec.xq[name], dec.xs[name], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
+                fp8.fp8_linear(dec.x[r][name], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
         g = capture(torch, gemms)
         t = time_graph(torch, g, 50) / dec.R
         per_layer[name] = t
         gemm_ms += t
-        gemm_b += gemm_bytes(M, N, K)
+        gemm_b += linear_bytes(M, N, K)
         del g
     have_ev = gemm_ms > 0
 
@@ -596,22 +603,23 @@ def main():
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out", "data": "synthetic",
         "config": {"workload": "decode linears wq_a 7168->1536, wq_b 1536->24576, wo 16384->7168; "
-                               "M=16 tokens; act_quant + fp8_gemm per layer",
+                               "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear, one kernel each)",
                    "global_batch": M * world, "parallelism": f"replicas x{world}",
                    "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
                    "launch": "CUDA graph per step"},
         "tflops": world * step_flops / (ms_per_step * 1e9),
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "e2e": e2e,
         "clocks": clocks,
         "peaks_source": peak_src,
     }
     if have_ev and gemm_ms > 0:
         achieved = gemm_b / gemm_ms / 1e6
-        line["roofline"] = {"kernel": "fp8_gemm (swap-AB, stream-K)", "bound": "hbm", "achieved": achieved,
+        line["roofline"] = {"kernel": "fp8_linear: act_quant fused into the swap-AB cluster split-K fp8 GEMM",
+                            "bound": "hbm", "achieved": achieved,
                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                             "peak_kind": f"{peak_src} copy bandwidth",
-                            "traffic": profiled_traffic("fp8_gemm", "decode_M16"),
+                            "traffic": profiled_traffic("fp8_linear", "decode_M16"),
                             "launch_us": {n: v * 1e3 for n, v in per_layer.items()},
                             "timing": "per layer: CUDA graph of its 4 rotation launches, events around 50 replays"}
     if rank == 0 and world == 1 and not args.no_cpu:

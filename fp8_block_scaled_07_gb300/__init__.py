@@ -49,6 +49,8 @@ def _declare(lib):
         "fp8_moe_route": (st, [vp, i64, i32, i32, vp, vp, vp, vp]),
         "fp8_moe_gather": (st, [vp, f32p, vp, i64, i64, vp, f32p, vp]),
         "fp8_moe_combine": (st, [vp, f32p, vp, i64, i32, i64, vp, f32p, vp]),
+        "fp8_linear_workspace_size": (sz, [i64, i64, i64]),
+        "fp8_linear": (st, [vp, vp, f32p, vp, f32p, i64, i64, i64, ctypes.c_int, vp, sz, vp]),
         "fp8_device_status": (st, [vp]),
         "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "fp8_num_sms": (ctypes.c_int, []),
@@ -284,7 +286,26 @@ def fp8_num_sms():
     return int(lib.fp8_num_sms())
 
 
-def fp8_linear(x, w, w_s, scale_fmt=FP8_SCALE_FP32, out_fp32=False, stream=None):
-    """The FP8 branch of the model's linear(): act_quant(x) then fp8_gemm."""
-    xq, xs = fp8_act_quant(x, scale_fmt, stream=stream)
-    return fp8_gemm(xq, xs, w, w_s, out_bf16=True, out_fp32=out_fp32, stream=stream)
+def fp8_linear(x, w, w_s, scale_fmt=FP8_SCALE_FP32, out_bf16=True, out_fp32=False, c_bf16=None,
+               c_fp32=None, workspace=None, stream=None):
+    """The FP8 branch of the model's linear(): act_quant(x) then fp8_gemm, in
+    one call (fused into one kernel for small decode batches).  Returns
+    (c_bf16 or None, c_fp32 or None)."""
+    _cuda(x, "x", _BF16, 2)
+    _cuda(w, "w", _E4M3, 2)
+    _cuda(w_s, "w_s", _F32, 2)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or tuple(w_s.shape) != ((N + BLOCK - 1) // BLOCK, K // BLOCK):
+        raise ValueError("shape mismatch")
+    if c_bf16 is None and out_bf16:
+        c_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if c_fp32 is None and out_fp32:
+        c_fp32 = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = torch.cuda.current_stream() if stream is None else stream
+    if workspace is None:
+        workspace = workspaces.get(int(lib.fp8_linear_workspace_size(M, N, K)), x.device, st)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("fp8_linear", lib.fp8_linear(_ptr(x), _ptr(w), _ptr(w_s), _ptr(c_bf16), _ptr(c_fp32), M, N, K,
+                                        int(scale_fmt), _ptr(workspace), ws_bytes, _stream(st)))
+    return c_bf16, c_fp32

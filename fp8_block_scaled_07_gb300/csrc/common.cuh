@@ -68,6 +68,60 @@ __device__ __forceinline__ float block_scale(float amax, bool ue8m0) {
     return ue8m0 ? pow2_ceil(s) : s;
 }
 
+// 8 bf16 (one 16-byte load) -> 8 fp32, exact.
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// x / s for 8 values, then RNE-satfinite e4m3, packed low byte first.  The
+// one quantisation routine of the library: act_quant, the fused expert body
+// and the fused decode linear all call it, so their codes agree bit for bit.
+//
+// The quotient must be the IEEE fp32 x / s rounded to nearest.  ue8m0 scales
+// are powers of two, so x * (1/s) is that quotient exactly.  For fp32 scales
+// the quotient is formed by Markstein's correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): r = RN(1/s), q0 = RN(x r), the
+// exact remainder e = x - q0 s by one fma, then q = RN(q0 + e r).  Here x is
+// a bf16 value and s = RN(max(|x|max, 1e-4) / 448) of its block, so x/s
+// depends only on the two 8-bit mantissas and their exponent gap; the
+// parity tests enumerate that whole domain against the oracle's IEEE
+// division.  A zero x keeps its sign.
+template <bool UE8M0>
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+    float q[8];
+    const float r = __frcp_rn(s);
+    if (UE8M0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(f[i], r);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q0 = __fmul_rn(f[i], r);
+            const float e = __fmaf_rn(-q0, s, f[i]);
+            const float q1 = __fmaf_rn(e, r, q0);
+            q[i] = f[i] == 0.0f ? f[i] : q1;
+        }
+    }
+    uint2 out;
+    out.x = static_cast<uint32_t>(f32x2_to_e4m3x2(q[0], q[1])) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[2], q[3])) << 16);
+    out.y = static_cast<uint32_t>(f32x2_to_e4m3x2(q[4], q[5])) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[6], q[7])) << 16);
+    return out;
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (the tensor core reading operands from shared memory).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

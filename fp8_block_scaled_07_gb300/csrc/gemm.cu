@@ -68,7 +68,11 @@ constexpr int kMaxGroups = 1024;
 constexpr int kMaxSkTiles = 4096;
 constexpr size_t kCounterBytes = kMaxSkTiles * sizeof(int);
 
-enum Variant { kDense = 0, kDenseSwap = 1, kGrouped = 2 };
+enum Variant { kDense = 0, kDenseSwap = 1, kGrouped = 2, kSwapFused = 3 };
+// swapped layout (weights on the 128-row MMA side); kSwapFused also
+// quantises the bf16 activations inside the kernel (act_quant fused)
+template <int V>
+constexpr bool is_swap() { return V == kDenseSwap || V == kSwapFused; }
 constexpr int kScaleChunk = 32;   // slabs of scale products staged at a time (swapped layout)
 
 struct Params {
@@ -90,6 +94,9 @@ struct Params {
     long long total_units;     // num_tiles * KB
     int trace_slot;            // profiling builds: which timeline buffer this launch fills
     int ksplit;                // >0: cluster split-K, CTA = (tile, K part), cluster of ksplit CTAs
+    const uint16_t* x;         // fused: bf16 activations [M, K]
+    long long K;               // fused: row stride of x
+    int ue8m0;                 // fused: activation scale format
 };
 
 struct Tile {
@@ -105,12 +112,15 @@ struct Seg {
 
 template <int BN, int V>
 struct Cfg {
-    static constexpr bool kSwap = (V == kDenseSwap);
+    static constexpr bool kFusedV = (V == kSwapFused);
+    static constexpr bool kSwap = is_swap<V>();
+    static constexpr bool kFused = kFusedV;
     static constexpr int kQTileBytes = BN * kBlock;
-    static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
+    static constexpr int kXTileBytes = kFusedV ? BN * kBlock * 2 : 0;   // fused: bf16 activation tile
+    static constexpr int kStageBytes = kPTileBytes + kQTileBytes + kXTileBytes;
     // small swapped tiles: 5 stages (80 KB of weights in flight) so that two
     // CTAs fit on an SM -- the next launch's CTAs start while this one drains
-    static constexpr int kStages = (kSwap && BN <= 32) ? 5 : (BN == 256 ? 4 : (BN >= 128 ? 6 : 7));
+    static constexpr int kStages = kFusedV ? 4 : ((kSwap && BN <= 32) ? 5 : (BN == 256 ? 4 : (BN >= 128 ? 6 : 7)));
     static constexpr int kMinBlocks = (kSwap && BN <= 32) ? 2 : 1;
     // 128x256 tiles: 8 epilogue warps, two per TMEM lane quarter, each owning
     // 128 of the 256 columns; their warpgroups take registers from warps 0-3
@@ -124,8 +134,11 @@ struct Cfg {
     // grouped: per-expert tile prefix; swapped: two chunks of staged scales
     // swapped: staged scales + the split-K receive buffer (128 x BN fp32)
     static constexpr int kRecvBytes = kSwap ? 128 * BN * 4 : 0;
+    // fused: ring of per-slab scale products handed from quantiser to epilogue
+    static constexpr int kRingSlots = kStages + 2;
     static constexpr int kExtraBytes =
-        V == kGrouped ? (kMaxGroups + 1 + 16) * 4 : (kSwap ? 2 * kScaleChunk * BN * 4 + kRecvBytes : 0);
+        V == kGrouped ? (kMaxGroups + 1 + 16) * 4
+                      : (kSwap ? 2 * kScaleChunk * BN * 4 + kRecvBytes + (kFused ? kRingSlots * BN * 4 : 0) : 0);
     static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes + kExtraBytes;
     // weight slabs each CTA prefetches into L2 before its inputs are ready
     static constexpr int kL2Prefetch = kStages;
@@ -207,7 +220,7 @@ __device__ __forceinline__ Tile tile_geom(const Params& p, int t, const int* s_p
         g.q_row0 = tq * BN;
         g.p_valid = min(128, p.M - g.p_row0);
         g.q_valid = min(BN, p.N - g.q_row0);
-    } else if (V == kDenseSwap) {
+    } else if (is_swap<V>()) {
         const int tp = t % p.tiles_p, tq = t / p.tiles_p;
         g.p_row0 = tp * 128;         // weight rows (output columns)
         g.q_row0 = tq * BN;          // token rows
@@ -244,7 +257,7 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
 template <int BN, int V, int CPT>
 __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int e, int cofs,
                                            const float (&acc)[CPT]) {
-    if (V == kDenseSwap) {
+    if (is_swap<V>()) {
         const int n = tg.p_row0 + e;
         if (e >= tg.p_valid) return;
 #pragma unroll
@@ -288,6 +301,66 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
                     if (p.c_fp32) p.c_fp32[row * p.N + col + i] = acc[j0 + i];
                 }
             }
+        }
+    }
+}
+
+// Fused act_quant for the swapped decode layout (BN == 16, 64 threads):
+// thread (r, sub) quantises values [32 sub, 32 sub + 32) of token row r of
+// each slab from the bf16 tile TMA placed in shared memory (two 64-column
+// halves, 128-byte swizzle); the four threads of a row share the block max
+// by shuffles.  Codes go to the stage's e4m3 tile in the layout the MMA
+// reads; the scale products b_s * a_s go to a ring the epilogue reads.
+template <int BN, int S>
+__device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, const int* s_prefix, uint8_t* sQ,
+                                               const uint8_t* sX, float* s_ring, uint64_t* full, uint64_t* xfull,
+                                               volatile int* abort_flag) {
+    static_assert(BN == 16, "fused quantisation covers 16-token tiles");
+    constexpr int kQTile = BN * kBlock, kXTile = BN * kBlock * 2, kRing = S + 2;
+    const int qt = threadIdx.x - 64, lane = threadIdx.x & 31;
+    const int r = qt >> 2, sub = qt & 3;
+    uint32_t iter = 0;
+    Seg sg;
+    while (it.next(sg)) {
+        const Tile tg = tile_geom<BN, kSwapFused>(p, sg.tile, s_prefix);
+        const bool valid = r < tg.q_valid;
+        const float* bs_row = p.b_s + static_cast<int64_t>(tg.p_row0 / 128) * p.KB;
+        float bsc = __ldg(bs_row + sg.k0);
+        for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
+            const float bsc_next = kb + 1 < sg.k1 ? __ldg(bs_row + kb + 1) : 0.0f;
+            const int st = iter % S;
+            if (!mbar_wait(&xfull[st], (iter / S) & 1, abort_flag)) {
+                set_abort(abort_flag);
+                return;
+            }
+            const uint8_t* xrow = sX + st * kXTile + (sub >> 1) * (kXTile / 2) + r * 128;
+            float f[4][8];
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = (sub & 1) * 4 + i;
+                unpack_bf16x8(*reinterpret_cast<const uint4*>(xrow + ((c ^ (r & 7)) * 16)), f[i]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[i][j]));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            const float sc = block_scale(amax, p.ue8m0 != 0);
+            uint2 q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                q[i] = p.ue8m0 ? quant8<true>(f[i], sc) : quant8<false>(f[i], sc);
+                if (!valid) q[i] = make_uint2(0, 0);
+            }
+            // 16-byte e4m3 chunks 2*sub and 2*sub+1 of row r, 128-byte swizzle
+            uint8_t* row = sQ + st * kQTile + r * 128;
+            *reinterpret_cast<uint4*>(row + (((2 * sub) ^ (r & 7)) * 16)) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+            *reinterpret_cast<uint4*>(row + (((2 * sub + 1) ^ (r & 7)) * 16)) = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
+            if (sub == 0) s_ring[(iter % kRing) * BN + r] = valid ? bsc * sc : 0.0f;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[st]);
+            bsc = bsc_next;
         }
     }
 }
@@ -383,6 +456,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sP = smem;                                   // S x 16 KB
     uint8_t* sQ = smem + S * kPTileBytes;                 // S x BN*128
+    uint8_t* sX = sQ + S * C::kQTileBytes;                // fused: S x (BN x 128 bf16, two swizzled halves)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
     uint64_t* full = bars;                 // S
     uint64_t* empty = bars + S;            // S
@@ -391,12 +465,14 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     uint64_t* mma_done = bars + 2 * S + 4; // 1
     uint64_t* epi_bar = bars + 2 * S + 5;  // epilogue-group barrier
     uint64_t* red_bar = bars + 2 * S + 6;  // cluster split-K: all partials pushed to this CTA
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 8);
+    uint64_t* xfull = bars + 2 * S + 8;    // fused: S barriers, activation tile landed
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
     int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kBarBytes);
     float* s_scale = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kBarBytes);
     float* s_recv = s_scale + 2 * kScaleChunk * BN;   // swapped: split-K partials pushed here
+    float* s_ring = s_recv + 128 * BN;                 // fused: per-slab scale products
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -404,8 +480,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], C::kFused ? 3 : 1);   // fused: TMA + two quantiser warps
             mbar_init(&empty[i], 1);
+            if (C::kFused) mbar_init(&xfull[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -430,7 +507,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             while (n < C::kL2Prefetch && pit.next(ps)) {
                 const Tile tg = tile_geom<BN, V>(p, ps.tile, nullptr);
                 for (int kb = ps.k0; kb < ps.k1 && n < C::kL2Prefetch; ++kb, ++n) {
-                    if (V == kDenseSwap) tma_prefetch_l2_2d(&tm_p, kb * kBlock, tg.p_row0);
+                    if (is_swap<V>()) tma_prefetch_l2_2d(&tm_p, kb * kBlock, tg.p_row0);
                     else tma_prefetch_l2_2d(&tm_q, kb * kBlock, tg.q_row0);
                 }
             }
@@ -484,9 +561,19 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                         break;
                     }
                     if (iter == 0) FP8BS_TRACE(2);
-                    mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-                    tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
-                    tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
+                    if constexpr (C::kFused) {
+                        // activation tile (two 64-column halves) for the quantiser
+                        mbar_arrive_expect_tx(&xfull[st], C::kXTileBytes);
+                        tma_load_2d(sX + st * C::kXTileBytes, &tm_q, &xfull[st], kb * kBlock, tg.q_row0);
+                        tma_load_2d(sX + st * C::kXTileBytes + C::kXTileBytes / 2, &tm_q, &xfull[st],
+                                    kb * kBlock + 64, tg.q_row0);
+                        mbar_arrive_expect_tx(&full[st], kPTileBytes);
+                        tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
+                    } else {
+                        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                        tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
+                        tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
+                    }
                 }
             }
             // drain: every load issued must land before the CTA may exit
@@ -528,6 +615,11 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             const volatile int never = 0;
             if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
         }
+    } else if (C::kFused) {
+        // ---------------------------------------------------------- quantiser
+        // warps 2-3: act_quant of the token rows of each slab, written as the
+        // e4m3 Q tile in the 128-byte-swizzled layout the MMA reads
+        if constexpr (C::kFused) quantiser_role<BN, S>(p, it, s_prefix, sQ, sX, s_ring, full, xfull, abort_flag);
     }
     } else {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
@@ -548,7 +640,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             }
             tc_fence_after();
             if (slab == 0 && e == 0) FP8BS_TRACE(4);
-            promote<CPT, V == kDenseSwap>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs),
+            promote<CPT, is_swap<V>()>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs),
                                           acc, sc_col, sc);
             tc_fence_before();
             mbar_arrive(&tempty[buf]);
@@ -560,7 +652,11 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             float acc[CPT];
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
-            if constexpr (V == kDenseSwap) {
+            if constexpr (V == kSwapFused) {
+                // scale products b_s[block] * a_s[token] come from the quantiser
+                for (int kb = sg.k0; kb < sg.k1 && ok; ++kb)
+                    ok = take_slab(acc, s_ring + (slab % C::kRingSlots) * BN, 0.0f);
+            } else if constexpr (V == kDenseSwap) {
                 // scale products b_s[block] * a_s[token] of 32 slabs at a time,
                 // staged in shared memory one chunk ahead
                 constexpr int CH = kScaleChunk, PER = CH * BN / 128;
@@ -631,7 +727,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
                 continue;
             }
-            if constexpr (V == kDenseSwap) {
+            if constexpr (is_swap<V>()) {
                 if (p.ksplit > 1) {
                     // ---- cluster split-K: every CTA pushes each tile row of its
                     // partial to the CTA that owns that row (rank = row / rows);
@@ -780,6 +876,21 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     });
     return fn;
+}
+
+// 2-D map over a bf16 matrix [rows, K] (row stride 2K bytes), box 64 x box_rows
+// (128-byte rows), 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 // 2-D map over an e4m3 matrix [rows, K] (row stride K bytes), box 128 x box_rows.
@@ -1087,4 +1198,81 @@ extern "C" fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const vo
     }
     return fp8_gemm(a, a_s, b, b_s, c_bf16, c_fp32, M, N, K, scratch, need > 0 ? kNoAllocScratchBytes : 0,
                     stream);
+}
+
+// ------------------------------------------------------------------ fused linear
+namespace {
+constexpr size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// The fused kernel saves the act_quant launch (~3 us on GB300) but every CTA
+// quantises its own slabs, redundantly across output tiles (~0.2-0.3 us per
+// slab on two warps): it is used when a CTA's K range is short.  Measured at
+// M=16: wq_a (7 slabs per CTA) 8.5 vs 9.0 us, wq_b (12) 12.8 vs 11.8 us,
+// wo (32) 28.9 vs 24.7 us for fused vs act_quant + fp8_gemm.
+constexpr int kFusedMaxSlabsPerCta = 8;
+
+bool linear_is_fused(int64_t M, int64_t N, int64_t K) {
+    if (M > 16) return false;
+    const Plan pl = make_plan(M, N, K, device_sm_count());
+    return pl.variant == kDenseSwap && pl.ksplit > 0 && pl.bn == 16 &&
+           (K / kBlock + pl.ksplit - 1) / pl.ksplit <= kFusedMaxSlabsPerCta;
+}
+}  // namespace
+
+extern "C" size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % kBlock != 0) return 0;
+    if (linear_is_fused(M, N, K)) return 0;
+    return align256(fp8_gemm_workspace_size(M, N, K)) + align256(static_cast<size_t>(M) * K) +
+           align256(static_cast<size_t>(M) * (K / kBlock) * 4);
+}
+
+extern "C" fp8_status fp8_linear(const void* x, const void* w, const float* w_s, void* c_bf16, float* c_fp32,
+                                 int64_t M, int64_t N, int64_t K, int scale_fmt, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (M < 0 || N < 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
+    if (scale_fmt != FP8_SCALE_FP32 && scale_fmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!x || !w || !w_s || (!c_bf16 && !c_fp32) || !aligned16(x) || !aligned16(w)) return FP8_ERR_INVALID_ARG;
+    if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!linear_is_fused(M, N, K)) {
+        const size_t need = fp8_linear_workspace_size(M, N, K);
+        if (!workspace || workspace_bytes < need) return FP8_ERR_WORKSPACE;
+        // layout: [fp8_gemm workspace (zero-kept counters first)][codes][scales],
+        // so a workspace shared with fp8_gemm keeps its counters in place
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        const size_t g_bytes = align256(fp8_gemm_workspace_size(M, N, K));
+        const size_t q_bytes = align256(static_cast<size_t>(M) * K);
+        uint8_t* xq = ws + g_bytes;
+        float* xs = reinterpret_cast<float*>(xq + q_bytes);
+        fp8_status r = fp8_act_quant(x, xq, xs, M, K, scale_fmt, stream);
+        if (r != FP8_OK) return r;
+        return fp8_gemm(xq, xs, w, w_s, c_bf16, c_fp32, M, N, K, g_bytes ? ws : nullptr, g_bytes, stream);
+    }
+    if ((c_bf16 && (reinterpret_cast<uintptr_t>(c_bf16) & 1)) || (c_fp32 && (reinterpret_cast<uintptr_t>(c_fp32) & 3)))
+        return FP8_ERR_INVALID_ARG;
+    const Plan pl = make_plan(M, N, K, device_sm_count());
+    Params prm{};
+    prm.b_s = w_s;
+    prm.c_bf16 = static_cast<__nv_bfloat16*>(c_bf16);
+    prm.c_fp32 = c_fp32;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.KB = static_cast<int>(K / kBlock);
+    prm.NB = static_cast<int>((N + 127) / 128);
+    prm.G = 1;
+    prm.tiles_p = pl.tiles_p;
+    prm.tiles_q = pl.tiles_q;
+    prm.num_tiles = pl.num_tiles;
+    prm.ksplit = pl.ksplit;
+    prm.x = static_cast<const uint16_t*>(x);
+    prm.K = K;
+    prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
+#ifdef FP8BS_TRACE_ENABLED
+    prm.trace_slot = g_trace_next++ & 3;
+#endif
+    CUtensorMap mp, mx;
+    if (!make_map(&mp, w, N, K, 128) || !make_map_bf16(&mx, x, M, K, 16)) return FP8_ERR_CUDA;
+    const cudaError_t e = launch<16, kSwapFused>(mp, mx, prm, pl.grid, st, pl.ksplit);
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }

@@ -24,14 +24,6 @@ constexpr int kUnroll = 4;   // independent 16-byte loads in flight per lane
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
 
 __device__ __forceinline__ float half_warp_max(float v) {
 #pragma unroll
@@ -39,27 +31,6 @@ __device__ __forceinline__ float half_warp_max(float v) {
     return v;
 }
 
-// x / s for the 8 values, then RNE-satfinite e4m3, packed low byte first.
-// ue8m0 scales are powers of two, so multiplying by the exact reciprocal
-// gives the same fp32 value as the division.
-template <bool UE8M0>
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
-    float q[8];
-    if (UE8M0) {
-        const float r = __frcp_rn(s);   // exact for a power of two
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = f[i] * r;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(f[i], s);
-    }
-    uint2 out;
-    out.x = static_cast<uint32_t>(f32x2_to_e4m3x2(q[0], q[1])) |
-            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[2], q[3])) << 16);
-    out.y = static_cast<uint32_t>(f32x2_to_e4m3x2(q[4], q[5])) |
-            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[6], q[7])) << 16);
-    return out;
-}
 
 template <bool UE8M0>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __restrict__ x,

@@ -104,6 +104,23 @@ fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float*
                     void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* The FP8 branch of the model's linear() (source tour, "FP8 with per-block
+ * scales": act_quant of the activations, then fp8_gemm against the e4m3
+ * weight and its block scales).  x [M, K] bf16 (device), w [N, K] e4m3,
+ * w_s [ceil(N/128), K/128] fp32 -> c_bf16 and/or c_fp32 [M, N].  scale_fmt
+ * is the activation scale format.  The result equals fp8_act_quant followed
+ * by fp8_gemm bit for bit.  For M <= 16 on decode shapes whose K is split
+ * into short ranges per CTA the quantisation runs inside the GEMM kernel (no
+ * workspace); otherwise the activation codes and scales are staged in the
+ * workspace, whose size
+ * fp8_linear_workspace_size() gives (0 when none is needed).  Layout:
+ * fp8_gemm's workspace first (same zero-fill rule), then codes and scales,
+ * so one workspace can serve both entry points in stream order. */
+size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+fp8_status fp8_linear(const void* x, const void* w, const float* w_s, void* c_bf16, float* c_fp32,
+                      int64_t M, int64_t N, int64_t K, int scale_fmt, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
 /* fp8_gemm without any allocation (the paper has no counterpart: this is a
  * convenience of this library).  For callers that cannot hand the library a
  * workspace -- code that must not call cudaMalloc on its hot path (it can

@@ -1,0 +1,86 @@
+"""GPU parity of fp8_linear, the model's FP8 linear in one call (source
+tour, "FP8 with per-block scales": act_quant of the activations, then
+fp8_gemm).  For small decode batches the quantisation runs inside the GEMM
+kernel; the result must equal act_quant followed by fp8_gemm bit for bit
+and match the oracle's exact block-scaled product."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests.helpers import check_gemm, dev_bf16, dev_e4m3, dev_f32, host_bits, host_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import fp8_block_scaled_07_gb300 as m
+    return m
+
+
+def _compare(fp8, x_bits, w_bits, ue8m0, what, expect_fused=None):
+    M, K = x_bits.shape
+    N = w_bits.shape[0]
+    fmt = fp8.FP8_SCALE_UE8M0 if ue8m0 else fp8.FP8_SCALE_FP32
+    if expect_fused is not None:
+        assert (fp8.lib.fp8_linear_workspace_size(M, N, K) == 0) == expect_fused
+    wq, ws = oracle.weight_quant(w_bits)
+    x = dev_bf16(x_bits)
+    w, w_s = dev_e4m3(wq), dev_f32(ws)
+    lb, lf = fp8.fp8_linear(x, w, w_s, fmt, out_bf16=True, out_fp32=True)
+    xq, xs = fp8.fp8_act_quant(x, fmt)
+    gb, gf = fp8.fp8_gemm(xq, xs, w, w_s, out_bf16=True, out_fp32=True)
+    fp8.fp8_device_status()
+    assert np.array_equal(host_f32(lf).view(np.uint32), host_f32(gf).view(np.uint32)), f"{what}: fp32 differs"
+    assert np.array_equal(host_bits(lb), host_bits(gb)), f"{what}: bf16 differs"
+    aq, as_ = oracle.act_quant(x_bits, ue8m0=ue8m0)
+    ref, mag = oracle.gemm(aq, as_, wq, ws)
+    check_gemm(ref, mag, host_f32(lf), host_bits(lb), what)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_decode_linears(fp8, M):
+    # wq_a splits K into short ranges per CTA (fused kernel); wq_b and wo
+    # stage the quantised activations in the workspace
+    for lin in syn.decode_linears(M):
+        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M={M}", expect_fused=(lin.name == "wq_a"))
+
+
+def test_fused_ue8m0_ragged_n(fp8):
+    lin = syn.ragged_ue8m0(16)
+    _compare(fp8, lin.x, lin.w, True, "wkv_a M=16 ue8m0", expect_fused=True)
+
+
+@pytest.mark.parametrize("K", [1024, 7168])
+def test_fused_short_k_ranges(fp8, K):
+    rng = np.random.default_rng(K)
+    x = syn.to_bf16_bits(rng.standard_normal((9, K)).astype(np.float32))
+    w = syn.to_bf16_bits(0.02 * rng.standard_normal((1280, K)).astype(np.float32))
+    _compare(fp8, x, w, False, f"9x1280x{K}", expect_fused=True)
+
+
+@pytest.mark.parametrize("M", [37, 2049])
+def test_staged_ragged_ue8m0(fp8, M):
+    lin = syn.ragged_ue8m0(M)
+    _compare(fp8, lin.x, lin.w, True, f"wkv_a M={M} ue8m0", expect_fused=False)
+
+
+def test_staged_mid_batch(fp8):
+    rng = np.random.default_rng(5)
+    x = syn.to_bf16_bits(rng.standard_normal((300, 1024)).astype(np.float32))
+    w = syn.to_bf16_bits(0.02 * rng.standard_normal((384, 1024)).astype(np.float32))
+    _compare(fp8, x, w, False, "300x384x1024", expect_fused=False)
+
+
+def test_fused_special_blocks(fp8):
+    # zero block, constant block and an outlier in the 16-token tile
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((16, 2048)).astype(np.float32)
+    x[0, :128] = 0.0
+    x[3, 128:256] = -2.5
+    x[15, 1900] = 3e4
+    w = 0.02 * rng.standard_normal((640, 2048)).astype(np.float32)
+    _compare(fp8, syn.to_bf16_bits(x), syn.to_bf16_bits(w), False, "special blocks", expect_fused=True)

@@ -126,3 +126,76 @@ def test_silu_mul_quant(fp8, ue8m0):
     yo, so = oracle.act_quant(g_gpu, ue8m0=ue8m0)
     assert np.array_equal(host_f32(s), so)
     assert np.array_equal(host_bits(y), yo)
+
+
+def _decision_point_blocks(seed, n_blocks):
+    """Blocks whose quotients x/s land on, and within a few fp32 ulps of,
+    every e4m3 rounding decision point (midpoints between neighbouring e4m3
+    values, incl. the subnormal ones and 2^-10) for varied scales."""
+    rng = np.random.default_rng(seed)
+    codes = np.arange(0x7F, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes)                       # 0 .. 448
+    mids = np.concatenate([(vals[:-1] + vals[1:]) / 2.0, [2.0 ** -10]])
+    rows = []
+    for _ in range(n_blocks):
+        amax = float(np.exp2(rng.uniform(-8, 8)))
+        amax = float(syn.bf16_bits_to_f32(syn.to_bf16_bits(np.array([amax], np.float32)))[0])
+        s = np.float32(np.float32(amax) / np.float32(448.0))
+        tgt = rng.choice(mids, size=127) * float(s) * (1.0 + rng.integers(-6, 7, size=127) * 2.0 ** -23)
+        tgt *= np.where(rng.random(127) < 0.5, -1.0, 1.0)
+        blk = np.concatenate([[amax], tgt]).astype(np.float32)
+        rows.append(blk)
+    x = np.stack(rows).reshape(n_blocks // 8, 8 * 128)
+    return syn.to_bf16_bits(x)
+
+
+def test_act_quant_at_rounding_decision_points(fp8):
+    # bf16 inputs cannot hit every midpoint exactly, but the rounding to bf16
+    # scatters them densely around the decision points of each block's scale
+    x = _decision_point_blocks(17, 4096)
+    _act_case(fp8, x, False)
+    _act_case(fp8, x, True)
+
+
+def _division_domain_blocks():
+    """Every (block-max mantissa, value mantissa, exponent gap 0..-22, sign)
+    combination: x / s for s = RN(amax / 448) is determined by these alone
+    (fp32 rounding is scale-free in the normal range and gaps below -22 give
+    code 0), plus every bf16 value below the 1e-4 floor against the floored
+    scale.  Returned as bf16 bit patterns [rows, 1024] (8 blocks per row)."""
+    m = np.arange(128, dtype=np.uint32)
+    blocks = []
+    for am in m:                                   # block max = (1 + am/128) * 2^0
+        amax_bits = np.uint16(0x3F80 | am)
+        vals = []
+        for gap in range(0, 23):
+            exp_field = 127 - gap
+            for sgn in (0, 0x8000):
+                vals.append((sgn | (exp_field << 7) | m).astype(np.uint16))
+        vals = np.concatenate(vals)
+        amax_f = syn.bf16_bits_to_f32(np.array([amax_bits], np.uint16))[0]
+        vals = vals[np.abs(syn.bf16_bits_to_f32(vals)) <= amax_f]
+        for i in range(0, len(vals), 127):
+            chunk = vals[i:i + 127]
+            blk = np.zeros(128, dtype=np.uint16)
+            blk[0] = amax_bits
+            blk[1:1 + len(chunk)] = chunk
+            blocks.append(blk)
+    # floored blocks: every positive and negative bf16 below 1e-4
+    small = np.arange(0, 0x38D1, dtype=np.uint32).astype(np.uint16)      # 0 .. just below 1e-4
+    small = small[syn.bf16_bits_to_f32(small) < 1e-4]
+    small = np.concatenate([small, small | np.uint16(0x8000)])
+    for i in range(0, len(small), 128):
+        blk = np.zeros(128, dtype=np.uint16)
+        chunk = small[i:i + 128]
+        blk[:len(chunk)] = chunk
+        blocks.append(blk)
+    blocks = np.stack(blocks)
+    pad = (-len(blocks)) % 8
+    if pad:
+        blocks = np.concatenate([blocks, np.zeros((pad, 128), np.uint16)])
+    return blocks.reshape(-1, 8 * 128)
+
+
+def test_act_quant_division_domain_exhaustive(fp8):
+    _act_case(fp8, _division_domain_blocks(), False)
