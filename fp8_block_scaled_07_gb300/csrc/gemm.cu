@@ -41,7 +41,13 @@ __device__ int g_gemm_status;   // FP8_OK or FP8_ERR_TIMEOUT, read by fp8_device
 // Optional per-CTA timeline (global timer, ns) for profiling builds only;
 // compiles to nothing unless FP8BS_TRACE_ENABLED is defined.
 #ifdef FP8BS_TRACE_ENABLED
-__device__ unsigned long long g_trace[4][512][12];
+__device__ unsigned long long g_trace[4][512][16];
+#define FP8BS_TRACE_VAL(slot, v)                                                      \
+    do {                                                                             \
+        if (blockIdx.x < 512) g_trace[p.trace_slot & 3][blockIdx.x][slot] = (v);     \
+    } while (0)
+#define FP8BS_TIC(v) const long long v = clock64()
+#define FP8BS_TOC(acc, v) acc += clock64() - (v)
 #define FP8BS_TRACE(slot)                                                            \
     do {                                                                             \
         if (blockIdx.x < 512) {                                                      \
@@ -54,6 +60,11 @@ __device__ unsigned long long g_trace[4][512][12];
 #define FP8BS_TRACE(slot) \
     do {                  \
     } while (0)
+#define FP8BS_TRACE_VAL(slot, v) \
+    do {                         \
+    } while (0)
+#define FP8BS_TIC(v)
+#define FP8BS_TOC(acc, v)
 #endif
 
 namespace {
@@ -97,6 +108,7 @@ struct Params {
     const uint16_t* x;         // fused: bf16 activations [M, K]
     long long K;               // fused: row stride of x
     int ue8m0;                 // fused: activation scale format
+    int tma_store;             // dense, bf16 only: full tiles leave through shared memory and TMA
 };
 
 struct Tile {
@@ -139,7 +151,12 @@ struct Cfg {
     static constexpr int kExtraBytes =
         V == kGrouped ? (kMaxGroups + 1 + 16) * 4
                       : (kSwap ? 2 * kScaleChunk * BN * 4 + kRecvBytes + (kFused ? kRingSlots * BN * 4 : 0) : 0);
-    static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kBarBytes + kExtraBytes;
+    // dense: per epilogue warp a 4 KB staging box (32 rows x 64 bf16, 128-byte
+    // swizzle) through which full output tiles leave by TMA stores
+    static constexpr bool kTmaStore = V == kDense;
+    static constexpr int kStgBytes = kTmaStore ? kEpiWarps * 4096 : 0;
+    static constexpr int kSmemBytes =
+        1024 /*align slack*/ + kStages * kStageBytes + kStgBytes + kBarBytes + kExtraBytes;
     // weight slabs each CTA prefetches into L2 before its inputs are ready
     static constexpr int kL2Prefetch = kStages;
 };
@@ -252,6 +269,10 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
     atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_TIMEOUT));
 }
 
+// True on every lane of the warp iff it is true on all of them: the outcome
+// of a bounded wait is made warp-uniform before any warp-collective step.
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xFFFFFFFFu, ok) != 0; }
+
 // Store the CPT accumulators of one output row starting at tile column
 // cofs (non-swapped layout) or of one output column (swapped layout).
 template <int BN, int V, int CPT>
@@ -305,6 +326,38 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
     }
 }
 
+// Store this warp's 32 output rows x CPT columns as bf16 through its 4 KB
+// staging buffer: lane = row, one TMA box of 32 rows x 64 columns at a time,
+// in the 128-byte-swizzled layout of the store's tensor map (16-byte chunk c
+// of row r sits at chunk c ^ (r % 8), so the warp's writes are conflict
+// free).  Rows and columns outside the output are clipped by the TMA unit.
+template <int CPT>
+__device__ __forceinline__ void store_tile_tma(const CUtensorMap* tm_c, uint8_t* stg, int lane, int col0, int row0,
+                                               const float (&acc)[CPT]) {
+#pragma unroll
+    for (int h = 0; h < CPT / 64; ++h) {
+        if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+        __syncwarp();
+        uint8_t* row = stg + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(acc[h * 64 + c * 8 + 2 * i], acc[h * 64 + c * 8 + 2 * i + 1]);
+                w[i] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm_c, stg, col0 + h * 64, row0);
+            bulk_commit();
+        }
+    }
+}
+
 // Fused act_quant for the swapped decode layout (BN == 16, 64 threads):
 // thread (r, sub) quantises values [32 sub, 32 sub + 32) of token row r of
 // each slab from the bf16 tile TMA placed in shared memory (two 64-column
@@ -329,7 +382,7 @@ __device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, cons
         for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
             const float bsc_next = kb + 1 < sg.k1 ? __ldg(bs_row + kb + 1) : 0.0f;
             const int st = iter % S;
-            if (!mbar_wait(&xfull[st], (iter / S) & 1, abort_flag)) {
+            if (!warp_all(mbar_wait(&xfull[st], (iter / S) & 1, abort_flag))) {
                 set_abort(abort_flag);
                 return;
             }
@@ -410,33 +463,46 @@ __device__ __forceinline__ void expert_tile_prefix(const int32_t* offsets, int G
 
 // Promote one finished slab from TMEM into the fp32 accumulators:
 // acc[j] += D[lane][j] * scale, the scale per column (smem, swapped layout)
-// or uniform for the row.
+// or uniform for the row.  Packed f32x2 FMAs (two IEEE round-to-nearest
+// FMAs per instruction, so the same values as scalar fmaf) halve the issue
+// slots of the promotion, which otherwise runs longer than the tensor core
+// takes for the next slab.
+template <int N, bool PER_COL>
+__device__ __forceinline__ void fma_chunk(float* acc, const uint32_t* r, const float* sc_col, float sc) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+        const float2 s2 = PER_COL ? *reinterpret_cast<const float2*>(sc_col + j) : make_float2(sc, sc);
+        const float2 v = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2,
+                                    make_float2(acc[j], acc[j + 1]));
+        acc[j] = v.x;
+        acc[j + 1] = v.y;
+    }
+}
+
 template <int BN, bool PER_COL>
 __device__ __forceinline__ void promote(uint32_t taddr, float (&acc)[BN], const float* sc_col, float sc) {
     if constexpr (BN == 16) {
         uint32_t r[16];
         tmem_ld16(taddr, r);
         tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = fmaf(__uint_as_float(r[j]), PER_COL ? sc_col[j] : sc, acc[j]);
+        fma_chunk<16, PER_COL>(acc, r, sc_col, sc);
     } else {
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t r[32];
             tmem_ld32(taddr + c0, r);
             tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                acc[c0 + j] = fmaf(__uint_as_float(r[j]), PER_COL ? sc_col[c0 + j] : sc, acc[c0 + j]);
+            fma_chunk<32, PER_COL>(acc + c0, r, PER_COL ? sc_col + c0 : nullptr, sc);
         }
     }
 }
 
-// Barrier of the 128 epilogue threads on an mbarrier (count 128) so that a
-// thread that gave up on a wait cannot leave the others blocked forever.
+// Barrier of the epilogue threads on an mbarrier (one arrival per thread) so
+// that a thread that gave up on a wait cannot leave the others blocked
+// forever; the warp's outcome is uniform.
 __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const volatile int* abort_flag) {
     mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase, abort_flag);
+    const bool ok = warp_all(mbar_wait(bar, phase, abort_flag));
     phase ^= 1u;
     if (!ok) {
         *const_cast<volatile int*>(abort_flag) = 1;
@@ -448,7 +514,7 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const v
 template <int BN, int V>
 __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlocks))
     gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
-                const Params p) {
+                const __grid_constant__ CUtensorMap tm_c, const Params p) {
     using C = Cfg<BN, V>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -457,7 +523,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     uint8_t* sP = smem;                                   // S x 16 KB
     uint8_t* sQ = smem + S * kPTileBytes;                 // S x BN*128
     uint8_t* sX = sQ + S * C::kQTileBytes;                // fused: S x (BN x 128 bf16, two swizzled halves)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+    uint8_t* sStg = smem + S * C::kStageBytes;           // dense: kEpiWarps x 4 KB output staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes + C::kStgBytes);
     uint64_t* full = bars;                 // S
     uint64_t* empty = bars + S;            // S
     uint64_t* tfull = bars + 2 * S;        // 2
@@ -469,8 +536,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
-    int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kBarBytes);
-    float* s_scale = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kBarBytes);
+    int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kStgBytes + C::kBarBytes);
+    float* s_scale = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kStgBytes + C::kBarBytes);
     float* s_recv = s_scale + 2 * kScaleChunk * BN;   // swapped: split-K partials pushed here
     float* s_ring = s_recv + 128 * BN;                 // fused: per-slab scale products
 
@@ -486,7 +553,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 32 * C::kEpiWarps);
+            mbar_init(&tempty[i], C::kEpiWarps);   // one arrival per epilogue warp
         }
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
@@ -551,15 +618,20 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         if (lane == 0) {
             uint32_t iter = 0;
             bool ok = true;
+#ifdef FP8BS_TRACE_ENABLED
+            long long w_empty = 0;
+#endif
             while (ok && it.next(sg)) {
                 const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
                 for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
                     const int st = iter % S;
+                    FP8BS_TIC(t0_);
                     if (!mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag)) {
                         set_abort(abort_flag);
                         ok = false;
                         break;
                     }
+                    FP8BS_TOC(w_empty, t0_);
                     if (iter == 0) FP8BS_TRACE(2);
                     if constexpr (C::kFused) {
                         // activation tile (two 64-column halves) for the quantiser
@@ -576,6 +648,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     }
                 }
             }
+            FP8BS_TRACE_VAL(11, static_cast<unsigned long long>(w_empty));
             // drain: every load issued must land before the CTA may exit
             for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
                 const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
@@ -589,12 +662,20 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
             uint32_t iter = 0, slab = 0;
             bool ok = true;
+#ifdef FP8BS_TRACE_ENABLED
+            long long w_tempty = 0, w_full = 0;
+#endif
             while (ok && it.next(sg)) {
                 for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter, ++slab) {
                     const int st = iter % S;
                     const int buf = slab & 1;
-                    if (!mbar_wait(&tempty[buf], ((slab >> 1) & 1) ^ 1, abort_flag) ||
-                        !mbar_wait(&full[st], (iter / S) & 1, abort_flag)) {
+                    FP8BS_TIC(t1_);
+                    const bool te = mbar_wait(&tempty[buf], ((slab >> 1) & 1) ^ 1, abort_flag);
+                    FP8BS_TOC(w_tempty, t1_);
+                    FP8BS_TIC(t2_);
+                    const bool fu = te && mbar_wait(&full[st], (iter / S) & 1, abort_flag);
+                    FP8BS_TOC(w_full, t2_);
+                    if (!te || !fu) {
                         set_abort(abort_flag);
                         ok = false;
                         break;
@@ -611,6 +692,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     mma_commit(&tfull[buf]);
                 }
             }
+            FP8BS_TRACE_VAL(12, static_cast<unsigned long long>(w_tempty));
+            FP8BS_TRACE_VAL(13, static_cast<unsigned long long>(w_full));
+            FP8BS_TRACE_VAL(14, static_cast<unsigned long long>(slab));
             mma_commit(mma_done);
             const volatile int never = 0;
             if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
@@ -632,18 +716,27 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         uint32_t slab = 0, epi_phase = 0, chunk_ctr = 0;
         bool ok = true;
         // one finished slab: wait for it in TMEM, promote it, free the buffer
+#ifdef FP8BS_TRACE_ENABLED
+        long long w_tfull = 0;
+#endif
+        // The buffer is handed back with one arrival per warp (a warp-wide
+        // arrival is 32 barrier updates on the MMA warp's critical path); the
+        // warp votes on its bounded waits so every lane leaves together.
         auto take_slab = [&](float (&acc)[CPT], const float* sc_col, float sc) -> bool {
             const int buf = slab & 1;
-            if (!mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag)) {
+            FP8BS_TIC(t3_);
+            if (!warp_all(mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag))) {
                 set_abort(abort_flag);
                 return false;
             }
+            FP8BS_TOC(w_tfull, t3_);
             tc_fence_after();
             if (slab == 0 && e == 0) FP8BS_TRACE(4);
             promote<CPT, is_swap<V>()>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs),
                                           acc, sc_col, sc);
             tc_fence_before();
-            mbar_arrive(&tempty[buf]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
             ++slab;
             return true;
         };
@@ -724,6 +817,13 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             if (!ok) break;
             if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
+                if constexpr (C::kTmaStore) {
+                    if (p.tma_store) {
+                        store_tile_tma<CPT>(&tm_c, sStg + (warp - kEpiWarp0) * 4096, lane,
+                                            tg.q_row0 + cofs, tg.p_row0 + q * 32, acc);
+                        continue;
+                    }
+                }
                 store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
                 continue;
             }
@@ -746,7 +846,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     // lane r of the first epilogue warp tells owner r; each release covers
                     // the pushes of every thread ordered before it by the barrier above
                     if (e < c) mbar_arrive_remote(cluster_map(smem_u32(red_bar), static_cast<uint32_t>(e)));
-                    if (!mbar_wait(red_bar, 0, abort_flag)) {
+                    if (!warp_all(mbar_wait(red_bar, 0, abort_flag))) {
                         set_abort(abort_flag);
                         ok = false;
                         break;
@@ -853,6 +953,13 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             }
             }
             if (e == 0) FP8BS_TRACE(6);
+        }
+#ifdef FP8BS_TRACE_ENABLED
+        if (e == 0 && cofs == 0) FP8BS_TRACE_VAL(15, static_cast<unsigned long long>(w_tfull));
+#endif
+        // the staging boxes must be read out before the CTA's shared memory goes
+        if constexpr (C::kTmaStore) {
+            if (lane == 0) bulk_wait_all();
         }
     }
 
@@ -975,8 +1082,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
 }
 
 template <int BN, int V>
-cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& prm, int grid,
-                   cudaStream_t st, unsigned cluster = 1) {
+cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorMap& mc, const Params& prm,
+                   int grid, cudaStream_t st, unsigned cluster = 1) {
     using C = Cfg<BN, V>;
     constexpr int smem = C::kSmemBytes;
     static int configured[64] = {0};
@@ -988,7 +1095,7 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const Params& p
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    return launch_pdl_cluster(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, cluster, mp, mq,
+    return launch_pdl_cluster(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, cluster, mp, mq, mc,
                               prm);
 }
 
@@ -1034,12 +1141,12 @@ using namespace fp8bs;
 #ifdef FP8BS_TRACE_ENABLED
 static int g_trace_next = 0;
 extern "C" int fp8_debug_clear_trace(void) {
-    static unsigned long long zero[4][512][12];
+    static unsigned long long zero[4][512][16];
     g_trace_next = 0;
     return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 extern "C" int fp8_debug_read_trace(unsigned long long* host) {
-    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * 4 * 512 * 12) == cudaSuccess ? 0 : 1;
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * 4 * 512 * 16) == cudaSuccess ? 0 : 1;
 }
 #endif
 
@@ -1088,23 +1195,27 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
         prm.counters = static_cast<int*>(workspace);
         prm.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
     }
-    CUtensorMap mp, mq;
+    CUtensorMap mp, mq, mc;
     const bool swap = pl.variant == kDenseSwap;
     // P: 128-row tiles; Q: BN-row tiles
     if (!make_map(&mp, swap ? b : a, swap ? N : M, K, 128) ||
         !make_map(&mq, swap ? a : b, swap ? M : N, K, pl.bn))
         return FP8_ERR_CUDA;
+    // C (dense, bf16 only, 16-byte rows): 32 x 64 boxes for the TMA tile store
+    prm.tma_store = (!swap && c_bf16 && !c_fp32 && N % 8 == 0) ? 1 : 0;
+    if (prm.tma_store && !make_map_bf16(&mc, c_bf16, M, N, 32)) return FP8_ERR_CUDA;
+    if (!prm.tma_store) mc = mp;   // not read
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (!swap) {
-        e = pl.bn == 256 ? launch<256, kDense>(mp, mq, prm, pl.grid, st)
-                         : launch<128, kDense>(mp, mq, prm, pl.grid, st);
+        e = pl.bn == 256 ? launch<256, kDense>(mp, mq, mc, prm, pl.grid, st)
+                         : launch<128, kDense>(mp, mq, mc, prm, pl.grid, st);
     } else if (pl.bn == 16) {
-        e = launch<16, kDenseSwap>(mp, mq, prm, pl.grid, st, pl.ksplit);
+        e = launch<16, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
     } else if (pl.bn == 32) {
-        e = launch<32, kDenseSwap>(mp, mq, prm, pl.grid, st, pl.ksplit);
+        e = launch<32, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
     } else {
-        e = launch<64, kDenseSwap>(mp, mq, prm, pl.grid, st, pl.ksplit);
+        e = launch<64, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
     }
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -1141,8 +1252,8 @@ extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const vo
         !make_map(&mq, b, static_cast<int64_t>(G) * N, K, wide ? 256 : 128))
         return FP8_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = wide ? launch<256, kGrouped>(mp, mq, prm, device_sm_count(), st)
-                         : launch<128, kGrouped>(mp, mq, prm, device_sm_count(), st);
+    cudaError_t e = wide ? launch<256, kGrouped>(mp, mq, mp, prm, device_sm_count(), st)
+                         : launch<128, kGrouped>(mp, mq, mp, prm, device_sm_count(), st);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -1273,6 +1384,6 @@ extern "C" fp8_status fp8_linear(const void* x, const void* w, const float* w_s,
 #endif
     CUtensorMap mp, mx;
     if (!make_map(&mp, w, N, K, 128) || !make_map_bf16(&mx, x, M, K, 16)) return FP8_ERR_CUDA;
-    const cudaError_t e = launch<16, kSwapFused>(mp, mx, prm, pl.grid, st, pl.ksplit);
+    const cudaError_t e = launch<16, kSwapFused>(mp, mx, mp, prm, pl.grid, st, pl.ksplit);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }

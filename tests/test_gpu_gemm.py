@@ -172,3 +172,25 @@ def test_one_workspace_serves_shapes_in_any_order(fp8):
         if rows is not None:
             cf_h, cb_h = cf_h[rows], cb_h[rows]
         check_gemm(ref, mag, cf_h, cb_h, f"{M}x{N}x{K} shared workspace")
+
+
+@pytest.mark.parametrize("shape", [(300, 392, 256), (1000, 1000, 384), (2048, 4864, 256), (4100, 4736, 256)])
+def test_bf16_only_output_tile_store(fp8, shape):
+    # bf16-only outputs of the non-swapped layout leave through shared memory
+    # and TMA stores: bit-identical to the direct stores of a call that also
+    # asks for fp32, clipped at the ragged edges (rows past M stay untouched)
+    M, N, K = shape
+    a, as_, b, bs = _random_case(M, N, K, 80 + M % 17)
+    args = (dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs))
+    pad = 8
+    sentinel = 0x7FBF
+    buf = torch.full((M + pad, N), sentinel, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    fp8.fp8_gemm(*args, out_bf16=True, c_bf16=buf[:M])
+    cb, cf = fp8.fp8_gemm(*args, out_bf16=True, out_fp32=True)
+    fp8.fp8_device_status()
+    got = host_bits(buf)
+    assert np.all(got[M:] == sentinel), "rows past M were written"
+    assert np.array_equal(got[:M], host_bits(cb)), f"{shape}: TMA-stored bf16 differs from direct stores"
+    rows = np.unique(np.r_[0, 1, 31, 32, 127, 128, M // 2, M - 33, M - 1])
+    ref, mag = oracle.gemm(a, as_, b, bs, rows=rows)
+    check_gemm(ref, mag, host_f32(cf)[rows], got[:M][rows], f"{shape} bf16-only")
