@@ -41,7 +41,7 @@ __device__ int g_gemm_status;   // FP8_OK or FP8_ERR_TIMEOUT, read by fp8_device
 // Optional per-CTA timeline (global timer, ns) for profiling builds only;
 // compiles to nothing unless FP8BS_TRACE_ENABLED is defined.
 #ifdef FP8BS_TRACE_ENABLED
-__device__ unsigned long long g_trace[4][512][16];
+__device__ unsigned long long g_trace[4][512][24];
 #define FP8BS_TRACE_VAL(slot, v)                                                      \
     do {                                                                             \
         if (blockIdx.x < 512) g_trace[p.trace_slot & 3][blockIdx.x][slot] = (v);     \
@@ -109,6 +109,7 @@ struct Params {
     long long K;               // fused: row stride of x
     int ue8m0;                 // fused: activation scale format
     int tma_store;             // dense, bf16 only: full tiles leave through shared memory and TMA
+    int vec_scales;            // scale rows are 16-byte aligned (K/128 % 4 == 0, aligned bases)
 };
 
 struct Tile {
@@ -717,27 +718,33 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         bool ok = true;
         // one finished slab: wait for it in TMEM, promote it, free the buffer
 #ifdef FP8BS_TRACE_ENABLED
-        long long w_tfull = 0;
+        long long w_tfull = 0, w_promote = 0, w_store = 0;
 #endif
         // The buffer is handed back with one arrival per warp (a warp-wide
-        // arrival is 32 barrier updates on the MMA warp's critical path); the
-        // warp votes on its bounded waits so every lane leaves together.
+        // arrival is 32 barrier updates on the MMA warp's critical path).
+        // Every lane takes its own bounded wait and then runs the
+        // warp-collective loads whatever the outcome (a buffer read too early
+        // only yields values that are discarded with the timeout status); the
+        // warp votes once at the end, so its lanes always leave together.
         auto take_slab = [&](float (&acc)[CPT], const float* sc_col, float sc) -> bool {
             const int buf = slab & 1;
             FP8BS_TIC(t3_);
-            if (!warp_all(mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag))) {
-                set_abort(abort_flag);
-                return false;
-            }
+            const bool got = mbar_wait(&tfull[buf], (slab >> 1) & 1, abort_flag);
             FP8BS_TOC(w_tfull, t3_);
             tc_fence_after();
             if (slab == 0 && e == 0) FP8BS_TRACE(4);
+            FP8BS_TIC(t4_);
             promote<CPT, is_swap<V>()>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs),
                                           acc, sc_col, sc);
+            FP8BS_TOC(w_promote, t4_);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
             ++slab;
+            if (!warp_all(got)) {
+                set_abort(abort_flag);
+                return false;
+            }
             return true;
         };
         while (ok && it.next(sg)) {
@@ -792,12 +799,24 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                                       : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + (tg.q_col0 + cofs) / 128) * p.KB;
                 constexpr int PF = CPT >= 128 ? 4 : 8;   // prefetch distance (slabs)
                 float cs[PF], na[PF], nb[PF];
+                // four slabs' scales per 16-byte load where the rows allow it
+                const bool vec = p.vec_scales && (sg.k0 % 4) == 0;
                 auto load_next = [&](int base) {
 #pragma unroll
-                    for (int i = 0; i < PF; ++i) {
-                        const int kb = base + i;
-                        na[i] = kb < sg.k1 ? __ldg(ps + kb) : 0.0f;
-                        nb[i] = kb < sg.k1 ? __ldg(qs + kb) : 0.0f;
+                    for (int i = 0; i < PF; i += 4) {
+                        if (vec && base + i + 4 <= sg.k1) {
+                            const float4 va = __ldg(reinterpret_cast<const float4*>(ps + base + i));
+                            const float4 vb = __ldg(reinterpret_cast<const float4*>(qs + base + i));
+                            na[i] = va.x; na[i + 1] = va.y; na[i + 2] = va.z; na[i + 3] = va.w;
+                            nb[i] = vb.x; nb[i + 1] = vb.y; nb[i + 2] = vb.z; nb[i + 3] = vb.w;
+                        } else {
+#pragma unroll
+                            for (int j = i; j < i + 4; ++j) {
+                                const int kb = base + j;
+                                na[j] = kb < sg.k1 ? __ldg(ps + kb) : 0.0f;
+                                nb[j] = kb < sg.k1 ? __ldg(qs + kb) : 0.0f;
+                            }
+                        }
                     }
                 };
                 load_next(sg.k0);
@@ -817,14 +836,17 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             if (!ok) break;
             if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
+                FP8BS_TIC(t5_);
                 if constexpr (C::kTmaStore) {
                     if (p.tma_store) {
                         store_tile_tma<CPT>(&tm_c, sStg + (warp - kEpiWarp0) * 4096, lane,
                                             tg.q_row0 + cofs, tg.p_row0 + q * 32, acc);
+                        FP8BS_TOC(w_store, t5_);
                         continue;
                     }
                 }
                 store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
+                FP8BS_TOC(w_store, t5_);
                 continue;
             }
             if constexpr (is_swap<V>()) {
@@ -955,7 +977,11 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             if (e == 0) FP8BS_TRACE(6);
         }
 #ifdef FP8BS_TRACE_ENABLED
-        if (e == 0 && cofs == 0) FP8BS_TRACE_VAL(15, static_cast<unsigned long long>(w_tfull));
+        if (e == 0 && cofs == 0) {
+            FP8BS_TRACE_VAL(15, static_cast<unsigned long long>(w_tfull));
+            FP8BS_TRACE_VAL(16, static_cast<unsigned long long>(w_promote));
+            FP8BS_TRACE_VAL(17, static_cast<unsigned long long>(w_store));
+        }
 #endif
         // the staging boxes must be read out before the CTA's shared memory goes
         if constexpr (C::kTmaStore) {
@@ -1141,12 +1167,12 @@ using namespace fp8bs;
 #ifdef FP8BS_TRACE_ENABLED
 static int g_trace_next = 0;
 extern "C" int fp8_debug_clear_trace(void) {
-    static unsigned long long zero[4][512][16];
+    static unsigned long long zero[4][512][24];
     g_trace_next = 0;
     return cudaMemcpyToSymbol(g_trace, zero, sizeof(zero)) == cudaSuccess ? 0 : 1;
 }
 extern "C" int fp8_debug_read_trace(unsigned long long* host) {
-    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * 4 * 512 * 16) == cudaSuccess ? 0 : 1;
+    return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * 4 * 512 * 24) == cudaSuccess ? 0 : 1;
 }
 #endif
 
@@ -1188,6 +1214,7 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     prm.stream_k = pl.stream_k;
     prm.total_units = pl.total_units;
     prm.ksplit = pl.ksplit;
+    prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(b_s)) ? 1 : 0;
 #ifdef FP8BS_TRACE_ENABLED
     prm.trace_slot = g_trace_next++ & 3;
 #endif
@@ -1246,6 +1273,7 @@ extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const vo
     prm.NB = static_cast<int>(N / 128);
     prm.G = G;
     prm.stream_k = 0;
+    prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(b_s)) ? 1 : 0;
     const bool wide = (N % 256 == 0) && wide_tiles_ok();
     CUtensorMap mp, mq;
     if (!make_map(&mp, a, R_max, K, 128) ||
