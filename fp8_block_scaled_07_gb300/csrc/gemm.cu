@@ -33,6 +33,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 namespace fp8bs {
 
@@ -141,7 +142,9 @@ struct Cfg {
     static constexpr int kThreads = 128 + 32 * kEpiWarps;
     static constexpr int kCPT = BN * 4 / kEpiWarps;   // accumulator columns per epilogue thread
     static constexpr bool kSplitRegs = kEpiWarps == 8;
-    static constexpr int kRegsLow = 40, kRegsHigh = 232;   // 40*128 + 232*256 = 168*384
+    // the producer and MMA warps keep their tile state in registers (spills
+    // there were reloaded every slab); 120*128 + 192*256 = 168*384
+    static constexpr int kRegsLow = 120, kRegsHigh = 192;
     static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,...,256}
     static constexpr int kBarBytes = 1024;
     // grouped: per-expert tile prefix; swapped: two chunks of staged scales
@@ -217,6 +220,26 @@ struct SegIter {
             u = end;
             return true;
         }
+        if (t >= num_tiles) return false;
+        s.tile = t;
+        s.k0 = 0;
+        s.k1 = KB;
+        t += stride;
+        return true;
+    }
+};
+
+// Whole tiles blockIdx.x + i * gridDim.x only: the 128x256 kernels, whose
+// producer and MMA warps run on a small register budget, never split K.
+struct DpIter {
+    int t, stride, num_tiles, KB;
+    __device__ void init(const Params& p, int ntiles) {
+        t = blockIdx.x;
+        stride = gridDim.x;
+        num_tiles = ntiles;
+        KB = p.KB;
+    }
+    __device__ bool next(Seg& s) {
         if (t >= num_tiles) return false;
         s.tile = t;
         s.k0 = 0;
@@ -607,7 +630,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     }
     if (threadIdx.x == 0) FP8BS_TRACE(1);
 
-    SegIter it;
+    using Iter = std::conditional_t<C::kSplitRegs, DpIter, SegIter>;
+    Iter it;
     it.init(p, num_tiles);
     Seg sg;
 
