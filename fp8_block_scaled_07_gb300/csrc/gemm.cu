@@ -354,12 +354,15 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
 // staging buffer: lane = row, one TMA box of 32 rows x 64 columns at a time,
 // in the 128-byte-swizzled layout of the store's tensor map (16-byte chunk c
 // of row r sits at chunk c ^ (r % 8), so the warp's writes are conflict
-// free).  Rows and columns outside the output are clipped by the TMA unit.
+// free).  Boxes wholly outside the output (rows_valid or cols_valid used
+// up) are skipped; the TMA unit clips the partial ones.
 template <int CPT>
 __device__ __forceinline__ void store_tile_tma(const CUtensorMap* tm_c, uint8_t* stg, int lane, int col0, int row0,
-                                               const float (&acc)[CPT]) {
+                                               int rows_valid, int cols_valid, const float (&acc)[CPT]) {
+    if (rows_valid <= 0) return;
 #pragma unroll
     for (int h = 0; h < CPT / 64; ++h) {
+        if (h * 64 >= cols_valid) break;
         if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
         __syncwarp();
         uint8_t* row = stg + lane * 128;
@@ -817,9 +820,10 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 ++chunk_ctr;
             } else {
                 // per-row a_s and per-block b_s, prefetched PF slabs ahead in registers
-                const float* ps = p.a_s + static_cast<int64_t>(tg.p_row0 + (e < tg.p_valid ? e : 0)) * p.KB;
+                const float* ps = p.a_s + static_cast<int64_t>(e < tg.p_valid ? tg.p_row0 + e : 0) * p.KB;
+                // (columns past N read the last block's scales; they are never stored)
                 const float* qs = (V == kDense)
-                                      ? p.b_s + static_cast<int64_t>((tg.q_row0 + cofs) / 128) * p.KB
+                                      ? p.b_s + static_cast<int64_t>(min((tg.q_row0 + cofs) / 128, p.NB - 1)) * p.KB
                                       : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + (tg.q_col0 + cofs) / 128) * p.KB;
                 constexpr int PF = CPT >= 128 ? 4 : 8;   // prefetch distance (slabs)
                 float cs[PF], na[PF], nb[PF];
@@ -863,8 +867,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 FP8BS_TIC(t5_);
                 if constexpr (C::kTmaStore) {
                     if (p.tma_store) {
-                        store_tile_tma<CPT>(&tm_c, sStg + (warp - kEpiWarp0) * 4096, lane,
-                                            tg.q_row0 + cofs, tg.p_row0 + q * 32, acc);
+                        store_tile_tma<CPT>(&tm_c, sStg + (warp - kEpiWarp0) * 4096, lane, tg.q_row0 + cofs,
+                                            tg.p_row0 + q * 32, tg.p_valid - q * 32, tg.q_valid - cofs, acc);
                         FP8BS_TOC(w_store, t5_);
                         continue;
                     }

@@ -87,15 +87,19 @@ def test_data_parallel_schedule(fp8):
     _run(fp8, a, as_, b, bs, rows=rows, what="data-parallel")
 
 
-def test_wide_tile_schedule_ragged(fp8):
-    # enough 128x256 tiles for whole-tile scheduling, ragged in M and N
-    M, N, K = 4100, 4736, 256
+@pytest.mark.parametrize("shape", [(4100, 4736, 256), (4300, 4864, 384)])
+def test_wide_tile_schedule_ragged(fp8, shape):
+    # enough 128x256 tiles for whole-tile scheduling, ragged in M (last tile
+    # with 4 or 76 valid rows) and in N (the last tile's upper 128 columns lie
+    # past N for 4736, not for 4864)
+    M, N, K = shape
     a = syn.random_e4m3_codes((M, K), 31)
     b = syn.random_e4m3_codes((N, K), 32)
     as_ = syn.random_scales((M, K // 128), 33)
     bs = syn.random_scales(((N + 127) // 128, K // 128), 34)
-    rows = np.r_[0:2, 127:129, 2047, 4095:4100]
-    _run(fp8, a, as_, b, bs, rows=rows, what="wide tiles")
+    rows = np.unique(np.r_[0:2, 127:129, 255:257, 2047, 4095:4098, 4223:4226, M - 3:M])
+    rows = rows[rows < M]
+    _run(fp8, a, as_, b, bs, rows=rows, what=f"wide tiles {shape}")
 
 
 def test_prefill_mlp_shapes_sampled(fp8):
