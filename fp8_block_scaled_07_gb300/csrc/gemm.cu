@@ -1384,12 +1384,20 @@ bool linear_is_fused(int64_t M, int64_t N, int64_t K) {
     return pl.variant == kDenseSwap && pl.ksplit > 0 && pl.bn == 16 &&
            (K / kBlock + pl.ksplit - 1) / pl.ksplit <= kFusedMaxSlabsPerCta;
 }
+
+// Staged fp8_linear workspace: [fp8_gemm's region][codes][scales].  The
+// region in front is never shorter than the split-tile counters, which must
+// stay zero for whichever later call shares the workspace, even when this
+// shape's own GEMM needs no workspace.
+size_t linear_gemm_region(int64_t M, int64_t N, int64_t K) {
+    return align256(std::max(fp8_gemm_workspace_size(M, N, K), kCounterBytes));
+}
 }  // namespace
 
 extern "C" size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kBlock != 0) return 0;
     if (linear_is_fused(M, N, K)) return 0;
-    return align256(fp8_gemm_workspace_size(M, N, K)) + align256(static_cast<size_t>(M) * K) +
+    return linear_gemm_region(M, N, K) + align256(static_cast<size_t>(M) * K) +
            align256(static_cast<size_t>(M) * (K / kBlock) * 4);
 }
 
@@ -1405,16 +1413,18 @@ extern "C" fp8_status fp8_linear(const void* x, const void* w, const float* w_s,
     if (!linear_is_fused(M, N, K)) {
         const size_t need = fp8_linear_workspace_size(M, N, K);
         if (!workspace || workspace_bytes < need) return FP8_ERR_WORKSPACE;
-        // layout: [fp8_gemm workspace (zero-kept counters first)][codes][scales],
+        // layout: [fp8_gemm region (zero-kept counters first)][codes][scales],
         // so a workspace shared with fp8_gemm keeps its counters in place
         uint8_t* ws = static_cast<uint8_t*>(workspace);
-        const size_t g_bytes = align256(fp8_gemm_workspace_size(M, N, K));
+        const size_t g_need = fp8_gemm_workspace_size(M, N, K);
+        const size_t g_bytes = linear_gemm_region(M, N, K);
         const size_t q_bytes = align256(static_cast<size_t>(M) * K);
         uint8_t* xq = ws + g_bytes;
         float* xs = reinterpret_cast<float*>(xq + q_bytes);
         fp8_status r = fp8_act_quant(x, xq, xs, M, K, scale_fmt, stream);
         if (r != FP8_OK) return r;
-        return fp8_gemm(xq, xs, w, w_s, c_bf16, c_fp32, M, N, K, g_bytes ? ws : nullptr, g_bytes, stream);
+        return fp8_gemm(xq, xs, w, w_s, c_bf16, c_fp32, M, N, K, g_need ? ws : nullptr, g_need ? g_bytes : 0,
+                        stream);
     }
     if ((c_bf16 && (reinterpret_cast<uintptr_t>(c_bf16) & 1)) || (c_fp32 && (reinterpret_cast<uintptr_t>(c_fp32) & 3)))
         return FP8_ERR_INVALID_ARG;

@@ -114,12 +114,14 @@ fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float*
  * workspace); otherwise the activation codes and scales are staged in the
  * workspace, whose size
  * fp8_linear_workspace_size() gives (0 when none is needed).  Layout:
- * fp8_gemm's workspace first (same zero-fill rule), then codes and scales,
- * so one workspace can serve both entry points in stream order. */
+ * fp8_gemm's workspace first (same zero-fill rule, and never shorter than
+ * its 16 KiB of split-tile counters), then codes and scales, so one
+ * workspace can serve both entry points and any shapes in stream order. */
 size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
 fp8_status fp8_linear(const void* x, const void* w, const float* w_s, void* c_bf16, float* c_fp32,
                       int64_t M, int64_t N, int64_t K, int scale_fmt, void* workspace,
                       size_t workspace_bytes, void* stream);
+
 
 /* fp8_gemm without any allocation (the paper has no counterpart: this is a
  * convenience of this library).  For callers that cannot hand the library a

@@ -59,6 +59,8 @@ def test_host_validation_rejects_bad_arguments(fp8):
     assert L.fp8_silu_mul_quant(NULL, NULL, 256, 4, 100, NULL, NULL, NULL, 0, NULL) == 1
     assert L.fp8_moe_route(NULL, 4, 8, 2000, NULL, NULL, NULL, NULL) == 1
     assert L.fp8_moe_combine(NULL, NULL, NULL, 4, 8, 12, NULL, NULL, NULL) == 1
+    # fp8_linear: unknown scale format
+    assert L.fp8_linear(NULL, NULL, NULL, NULL, NULL, 4, 4, 128, 7, NULL, 0, NULL) == 1
 
 
 def test_empty_problems_are_no_ops(fp8):

@@ -84,3 +84,24 @@ def test_fused_special_blocks(fp8):
     x[15, 1900] = 3e4
     w = 0.02 * rng.standard_normal((640, 2048)).astype(np.float32)
     _compare(fp8, syn.to_bf16_bits(x), syn.to_bf16_bits(w), False, "special blocks", expect_fused=True)
+
+
+def test_staged_workspace_keeps_counters_clear(fp8):
+    # one workspace, staged calls in a row: wq_a's GEMM needs no workspace of
+    # its own, wq_b's (M=33) splits tiles through the workspace counters, which
+    # the first call's staged codes must not have touched
+    M = 33
+    lins = syn.decode_linears(M, layers=["wq_a", "wq_b"])
+    need = max(int(fp8.lib.fp8_linear_workspace_size(M, l.w.shape[0], l.w.shape[1])) for l in lins)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for lin in lins:
+        wq, wsc = oracle.weight_quant(lin.w)
+        x, w, w_s = dev_bf16(lin.x), dev_e4m3(wq), dev_f32(wsc)
+        outs.append((lin, wq, wsc, fp8.fp8_linear(x, w, w_s, out_bf16=True, out_fp32=True, workspace=ws)))
+    fp8.fp8_device_status()
+    assert int(ws[:16384].abs().sum()) == 0, "split-tile counters left non-zero"
+    for lin, wq, wsc, (lb, lf) in outs:
+        aq, as_ = oracle.act_quant(lin.x)
+        ref, mag = oracle.gemm(aq, as_, wq, wsc)
+        check_gemm(ref, mag, host_f32(lf), host_bits(lb), f"{lin.name} M={M} shared workspace")
