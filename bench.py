@@ -4,10 +4,11 @@ Workload of the headline line: DeepSeek-V3 decode-shaped linears at batch
 M=16 tokens -- wq_a (7168->1536), wq_b (1536->24576), wo (16384->7168) --
 with bf16 activations ~N(0,1) (0.5% outliers x30) and e4m3 weights with
 128x128 fp32 block scales drawn from N(0, 0.02).  One step = act_quant +
-fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer
-(the quantisation runs inside the GEMM kernel at this batch), replayed from
-CUDA graphs.  Four weight sets (4 x 167 MB) rotate between steps so every step
-streams its weights from HBM (inputs larger than L2).
+fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer:
+wq_a runs as one kernel (the quantisation inside the GEMM), wq_b and wo as
+an act_quant kernel followed by the GEMM kernel -- five launches, replayed
+from CUDA graphs.  Four weight sets (4 x 167 MB) rotate between steps so
+every step streams its weights from HBM (inputs larger than L2).
 
 value  = algorithmic HBM bytes of the step / device time (GB/s); the
          algorithmic bytes are what the method must move at least: e4m3
@@ -15,9 +16,12 @@ value  = algorithmic HBM bytes of the step / device time (GB/s); the
 e2e    = same metric through the Python binding with host buffers: each
          step copies the activations host->device, runs the three calls
          and copies the outputs device->host;
-roofline = the fused linear kernel (the only kernel of the step): per-launch
-         CUDA-event durations of graphs that replay only that layer's
-         launches (four weight rotations), taken right after the timed region;
+roofline = the dominant kernel, wo's GEMM (the largest share of the step in
+         the ncu launch list): its algorithmic bytes per launch over its
+         per-launch duration, from CUDA events around a graph of its four
+         weight-rotation launches (activations quantised beforehand),
+         replayed right after the timed region; the other layers' GEMM
+         kernels are timed the same way and listed beside it;
 cpu_baseline = the CPU oracle on the host cores over a bounded sample.
 
 With --impl reference the CPU oracle itself is timed on the same workload
@@ -464,6 +468,59 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ main
+# ------------------------------------------------------------------ ncu cases
+def _ncu_rand_e4m3(torch, shape, gen):
+    return torch.randint(0, 126, shape, dtype=torch.uint8, device="cuda", generator=gen).view(torch.float8_e4m3fn)
+
+
+def _ncu_gemm(fp8, torch, M, N, K):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    a = _ncu_rand_e4m3(torch, (M, K), gen)
+    b = _ncu_rand_e4m3(torch, (N, K), gen)
+    a_s = torch.rand((M, K // 128), device="cuda", generator=gen) + 0.5
+    b_s = torch.rand(((N + 127) // 128, K // 128), device="cuda", generator=gen) + 0.5
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        fp8.fp8_gemm(a, a_s, b, b_s, c_bf16=c)
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+
+def _ncu_linear(fp8, torch, M, N, K):
+    x = syn.normal_bf16_device((M, K), 1.0, 11, "cuda", outlier_frac=0.005, outlier_mult=30.0)
+    w, w_s = fp8.fp8_weight_quant(syn.normal_bf16_device((N, K), 0.02, 12, "cuda"))
+    for _ in range(3):
+        fp8.fp8_linear(x, w, w_s)
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+
+def _ncu_act_quant(fp8, torch):
+    x = syn.normal_bf16_device((4096, 18432), 1.0, 13, "cuda")
+    for _ in range(3):
+        fp8.fp8_act_quant(x)
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+
+def _ncu_dequant(fp8, torch):
+    w, s = fp8.fp8_weight_quant(syn.normal_bf16_device(syn.DEQUANT_SHAPE, 0.02, 14, "cuda"))
+    for _ in range(3):
+        fp8.fp8_weight_dequant(w, s)
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+
+NCU_CASES = {
+    "decode_wo": lambda fp8, torch: _ncu_gemm(fp8, torch, 16, *syn.DECODE_LAYERS["wo"]),
+    "decode_wq_a_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wq_a"]),
+    "prefill_w13": lambda fp8, torch: _ncu_gemm(fp8, torch, 4096, 2 * syn.MLP_INTER, syn.MLP_DIM),
+    "act_quant": _ncu_act_quant,
+    "weight_dequant": _ncu_dequant,
+}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,6 +533,10 @@ def main():
     ap.add_argument("--only-rows", default="",
                     help="comma list (act_quant,weight_dequant,ragged,prefill_mlp,moe): run just these "
                          "rows and print them (for profiling)")
+    ap.add_argument("--no-layer-timing", action="store_true",
+                    help="skip the per-layer GEMM timing after the timed region (profiling the step alone)")
+    ap.add_argument("--ncu-case", default="", choices=[""] + sorted(NCU_CASES),
+                    help="launch one kernel three times on a fixed workload and exit (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -499,6 +560,9 @@ def main():
 
     torch.cuda.set_device(local)
     import fp8_block_scaled_07_gb300 as fp8
+    if args.ncu_case:
+        NCU_CASES[args.ncu_case](fp8, torch)
+        return
     peaks, peak_src = load_peaks()
     if args.only_rows:
         print(json.dumps({"rows": rows_measurements(fp8, torch, peaks, set(args.only_rows.split(",")))}),
@@ -535,23 +599,28 @@ def main():
     ms = t_start.elapsed_time(t_end)
     fp8.fp8_device_status()
 
-    # per-launch durations of the fused linear kernel: per layer, a graph of
-    # its launches over the four weight rotations, events around replays
-    gemm_ms, gemm_b, per_layer = 0.0, 0, {}
+    # per-launch durations of each layer's GEMM kernel: a graph of its
+    # launches over the four weight rotations (activations quantised
+    # beforehand), events around 50 replays
+    per_layer = {}
+    launches_per_step = 0
     for name in LAYERS:
         N, K = syn.DECODE_LAYERS[name]
+        launches_per_step += 1 if int(fp8.lib.fp8_linear_workspace_size(M, N, K)) == 0 else 2
+        if args.no_layer_timing:
+            continue
+        xq = [fp8.fp8_act_quant(dec.x[r][name]) for r in range(dec.R)]
 
-        def gemms(name=name):
+        def gemms(name=name, xq=xq):
             for r in range(dec.R):
                 wq, wsc = dec.w[r][name]
-                fp8.fp8_linear(dec.x[r][name], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
+                fp8.fp8_gemm(xq[r][0], xq[r][1], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
         g = capture(torch, gemms)
-        t = time_graph(torch, g, 50) / dec.R
-        per_layer[name] = t
-        gemm_ms += t
-        gemm_b += linear_bytes(M, N, K)
+        per_layer[name] = time_graph(torch, g, 50) / dec.R
         del g
-    have_ev = gemm_ms > 0
+    fp8.fp8_device_status()
+    dom = max(per_layer, key=per_layer.get) if per_layer else None
+    have_ev = dom is not None and per_layer[dom] > 0
 
     ms_max = ms
     if pg:
@@ -603,25 +672,32 @@ def main():
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out", "data": "synthetic",
         "config": {"workload": "decode linears wq_a 7168->1536, wq_b 1536->24576, wo 16384->7168; "
-                               "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear, one kernel each)",
+                               "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear: one fused kernel "
+                               "for wq_a, act_quant + GEMM kernels for wq_b and wo)",
                    "global_batch": M * world, "parallelism": f"replicas x{world}",
                    "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
                    "launch": "CUDA graph per step"},
         "tflops": world * step_flops / (ms_per_step * 1e9),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
         "clocks": clocks,
         "peaks_source": peak_src,
     }
-    if have_ev and gemm_ms > 0:
-        achieved = gemm_b / gemm_ms / 1e6
-        line["roofline"] = {"kernel": "fp8_linear: act_quant fused into the swap-AB cluster split-K fp8 GEMM",
+    if have_ev:
+        N, K = syn.DECODE_LAYERS[dom]
+        achieved = gemm_bytes(M, N, K) / per_layer[dom] / 1e6
+        line["roofline"] = {"kernel": f"fp8_gemm {dom} ({N}x{K}, M={M}): swap-AB cluster split-K GEMM",
                             "bound": "hbm", "achieved": achieved,
                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                            "peak_kind": f"{peak_src} copy bandwidth",
-                            "traffic": profiled_traffic("fp8_linear", "decode_M16"),
-                            "launch_us": {n: v * 1e3 for n, v in per_layer.items()},
-                            "timing": "per layer: CUDA graph of its 4 rotation launches, events around 50 replays"}
+                            "peak_kind": f"{peak_src} copy bandwidth (burst)",
+                            "traffic": profiled_traffic("fp8_gemm", f"{dom}_M{M}"),
+                            "algorithmic_bytes_per_launch": gemm_bytes(M, N, K),
+                            "launch_us": per_layer[dom] * 1e3,
+                            "gemm_launch_us": {n: v * 1e3 for n, v in per_layer.items()},
+                            "gemm_GBps": {n: gemm_bytes(M, *syn.DECODE_LAYERS[n]) / v / 1e6
+                                          for n, v in per_layer.items()},
+                            "timing": "per layer: CUDA graph of its 4 weight-rotation GEMM launches, "
+                                      "events around 50 replays, right after the timed region"}
     if rank == 0 and world == 1 and not args.no_cpu:
         secs, nb, fl = oracle_decode_sample(torch, dec, 16)
         line["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": omp_threads(), "kind": "oracle",
