@@ -62,10 +62,27 @@ __device__ __forceinline__ float pow2_ceil(float s) {
     return __uint_as_float((u & 0x7F800000u) + 0x00800000u);
 }
 
-// The block scale: clamped max / 448 (IEEE divide), optionally ue8m0.
+// The block scale: clamped max / 448 rounded to nearest (as an IEEE
+// divide), optionally ue8m0.  amax is always the magnitude of a bf16 value
+// (or below the floor); on that domain one Markstein correction of
+// amax * RN(1/448) -- remainder by fma, then fma update (P. Markstein, IBM J.
+// Res. Dev. 34(1), 1990) -- gives the correctly rounded quotient for every
+// value, which the GPU tests check against the oracle's division block max by
+// block max.
 __device__ __forceinline__ float block_scale(float amax, bool ue8m0) {
-    float s = __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4m3Max);
+    constexpr float r = 1.0f / kE4m3Max;   // RN(1/448), folded at compile time
+    const float a = fmaxf(amax, kAmaxFloor);
+    const float q0 = __fmul_rn(a, r);
+    const float e = __fmaf_rn(-q0, kE4m3Max, a);
+    const float s = __fmaf_rn(e, r, q0);
     return ue8m0 ? pow2_ceil(s) : s;
+}
+
+// max |f[i]| over 8 values as a tree (max is exact, so the order is free).
+__device__ __forceinline__ float max_abs8(const float (&f)[8]) {
+    const float m0 = fmaxf(fabsf(f[0]), fabsf(f[1])), m1 = fmaxf(fabsf(f[2]), fabsf(f[3]));
+    const float m2 = fmaxf(fabsf(f[4]), fabsf(f[5])), m3 = fmaxf(fabsf(f[6]), fabsf(f[7]));
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
 // 8 bf16 (one 16-byte load) -> 8 fp32, exact.

@@ -415,14 +415,12 @@ __device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, cons
             }
             const uint8_t* xrow = sX + st * kXTile + (sub >> 1) * (kXTile / 2) + r * 128;
             float f[4][8];
-            float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int c = (sub & 1) * 4 + i;
                 unpack_bf16x8(*reinterpret_cast<const uint4*>(xrow + ((c ^ (r & 7)) * 16)), f[i]);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[i][j]));
             }
+            float amax = fmaxf(fmaxf(max_abs8(f[0]), max_abs8(f[1])), fmaxf(max_abs8(f[2]), max_abs8(f[3])));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
             const float sc = block_scale(amax, p.ue8m0 != 0);

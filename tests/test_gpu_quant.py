@@ -199,3 +199,29 @@ def _division_domain_blocks():
 
 def test_act_quant_division_domain_exhaustive(fp8):
     _act_case(fp8, _division_domain_blocks(), False)
+
+
+def _every_block_max_blocks(seed):
+    """One 128-block per finite bf16 magnitude (+0 .. 0x7F7F as bit
+    patterns), that magnitude being the block's max |x| (random sign and
+    position); the other 127 values are random bf16 no larger in magnitude,
+    random signs.  Returned as bf16 bit patterns [rows, 128]."""
+    rng = np.random.default_rng(seed)
+    mags = np.arange(0, 0x7F80, dtype=np.int64)
+    n = len(mags)
+    others = (rng.random((n, 127)) * (mags[:, None] + 1)).astype(np.int64)
+    signs = rng.integers(0, 2, size=(n, 128)).astype(np.int64) << 15
+    x = np.empty((n, 128), dtype=np.int64)
+    pos = rng.integers(0, 128, size=n)
+    x[:, :127] = others
+    x[:, 127] = mags
+    idx = np.arange(128)[None, :]
+    x = np.where(idx == pos[:, None], mags[:, None], np.where(idx < pos[:, None], x, np.roll(x, 1, axis=1)))
+    return (x | signs).astype(np.uint16)
+
+
+@pytest.mark.parametrize("ue8m0", [False, True])
+def test_act_quant_scale_for_every_bf16_block_max(fp8, ue8m0):
+    # the scale RN(max(amax, 1e-4) / 448) on its whole domain: every finite
+    # bf16 magnitude is the max of one block; scales and codes bit-exact
+    _act_case(fp8, _every_block_max_blocks(61 + ue8m0), ue8m0)
