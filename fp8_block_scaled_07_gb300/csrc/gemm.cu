@@ -155,10 +155,12 @@ struct Cfg {
     static constexpr int kExtraBytes =
         V == kGrouped ? (kMaxGroups + 1 + 16) * 4
                       : (kSwap ? 2 * kScaleChunk * BN * 4 + kRecvBytes + (kFused ? kRingSlots * BN * 4 : 0) : 0);
-    // dense: per epilogue warp a 4 KB staging box (32 rows x 64 bf16, 128-byte
-    // swizzle) through which full output tiles leave by TMA stores
-    static constexpr bool kTmaStore = V == kDense;
-    static constexpr int kStgBytes = kTmaStore ? kEpiWarps * 4096 : 0;
+    // dense / grouped: per epilogue warp a staging box (kStgRows rows x 64
+    // bf16, 128-byte swizzle) through which output tiles leave by TMA stores;
+    // 32 rows dense, 16 grouped (whose expert-tile prefix takes the room)
+    static constexpr bool kTmaStore = V == kDense || V == kGrouped;
+    static constexpr int kStgRows = V == kGrouped ? 16 : 32;
+    static constexpr int kStgBytes = kTmaStore ? kEpiWarps * kStgRows * 128 : 0;
     static constexpr int kSmemBytes =
         1024 /*align slack*/ + kStages * kStageBytes + kStgBytes + kBarBytes + kExtraBytes;
     // weight slabs each CTA prefetches into L2 before its inputs are ready
@@ -350,39 +352,54 @@ __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int 
     }
 }
 
-// Store this warp's 32 output rows x CPT columns as bf16 through its 4 KB
-// staging buffer: lane = row, one TMA box of 32 rows x 64 columns at a time,
-// in the 128-byte-swizzled layout of the store's tensor map (16-byte chunk c
-// of row r sits at chunk c ^ (r % 8), so the warp's writes are conflict
-// free).  Boxes wholly outside the output (rows_valid or cols_valid used
-// up) are skipped; the TMA unit clips the partial ones.
-template <int CPT>
-__device__ __forceinline__ void store_tile_tma(const CUtensorMap* tm_c, uint8_t* stg, int lane, int col0, int row0,
-                                               int rows_valid, int cols_valid, const float (&acc)[CPT]) {
-    if (rows_valid <= 0) return;
+// Store this warp's 32 output rows x CPT columns as bf16 through its
+// staging buffer: lane = row, one TMA box of ROWS rows x 64 columns at a
+// time (ROWS = 32, or 16: the two halves of the warp in turn), in the
+// 128-byte-swizzled layout of the store's tensor map (16-byte chunk c of row
+// r sits at chunk c ^ (r % 8), so the writes are conflict free).  Boxes
+// wholly outside the output (rows_valid or cols_valid used up) are skipped;
+// the TMA unit clips partial ones at the tensor's edge.  With ROWS = 16 a
+// half with fewer than 16 valid rows (a tile ending inside it, as grouped
+// tiles do at expert boundaries) is not stored here: the caller stores those
+// rows directly; the return value is that half's first row (or 32 if none).
+template <int CPT, int ROWS>
+__device__ __forceinline__ int store_tile_tma(const CUtensorMap* tm_c, uint8_t* stg, int lane, int col0, int row0,
+                                              int rows_valid, int cols_valid, const float (&acc)[CPT]) {
+    if (rows_valid <= 0) return 32;
 #pragma unroll
-    for (int h = 0; h < CPT / 64; ++h) {
-        if (h * 64 >= cols_valid) break;
-        if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
-        __syncwarp();
-        uint8_t* row = stg + lane * 128;
+    for (int h0 = 0; h0 < 32; h0 += ROWS) {
+        if (h0 >= rows_valid) return 32;
+        if (ROWS < 32 && rows_valid < h0 + ROWS) return h0;   // partial half: direct stores
+        const bool mine = lane >= h0 && lane < h0 + ROWS;
+        const int rr = lane - h0;                              // row within the box
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t w[4];
+        for (int h = 0; h < CPT / 64; ++h) {
+            if (h * 64 >= cols_valid) break;
+            if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+            __syncwarp();
+            if (mine) {
+                uint8_t* row = stg + rr * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 b = __floats2bfloat162_rn(acc[h * 64 + c * 8 + 2 * i], acc[h * 64 + c * 8 + 2 * i + 1]);
-                w[i] = *reinterpret_cast<uint32_t*>(&b);
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __nv_bfloat162 b =
+                            __floats2bfloat162_rn(acc[h * 64 + c * 8 + 2 * i], acc[h * 64 + c * 8 + 2 * i + 1]);
+                        w[i] = *reinterpret_cast<uint32_t*>(&b);
+                    }
+                    *reinterpret_cast<uint4*>(row + ((c ^ (rr & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
             }
-            *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tm_c, stg, col0 + h * 64, row0);
-            bulk_commit();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tm_c, stg, col0 + h * 64, row0 + h0);
+                bulk_commit();
+            }
         }
     }
+    return 32;
 }
 
 // Fused act_quant for the swapped decode layout (BN == 16, 64 threads):
@@ -865,8 +882,12 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 FP8BS_TIC(t5_);
                 if constexpr (C::kTmaStore) {
                     if (p.tma_store) {
-                        store_tile_tma<CPT>(&tm_c, sStg + (warp - kEpiWarp0) * 4096, lane, tg.q_row0 + cofs,
-                                            tg.p_row0 + q * 32, tg.p_valid - q * 32, tg.q_valid - cofs, acc);
+                        const int col0 = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) + cofs;
+                        const int rest = store_tile_tma<CPT, C::kStgRows>(
+                            &tm_c, sStg + (warp - kEpiWarp0) * (C::kStgRows * 128), lane, col0, tg.p_row0 + q * 32,
+                            tg.p_valid - q * 32, tg.q_valid - cofs, acc);
+                        // rows of a half the boxes left out (expert boundary): direct
+                        if (lane >= rest) store_tile<BN, V, CPT>(p, tg, e, cofs, acc);
                         FP8BS_TOC(w_store, t5_);
                         continue;
                     }
@@ -1301,13 +1322,17 @@ extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const vo
     prm.stream_k = 0;
     prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(b_s)) ? 1 : 0;
     const bool wide = (N % 256 == 0) && wide_tiles_ok();
-    CUtensorMap mp, mq;
+    CUtensorMap mp, mq, mc;
     if (!make_map(&mp, a, R_max, K, 128) ||
         !make_map(&mq, b, static_cast<int64_t>(G) * N, K, wide ? 256 : 128))
         return FP8_ERR_CUDA;
+    // bf16-only output: 16 x 64 boxes for the TMA tile store
+    prm.tma_store = (c_bf16 && !c_fp32) ? 1 : 0;
+    if (prm.tma_store && !make_map_bf16(&mc, c_bf16, R_max, N, 16)) return FP8_ERR_CUDA;
+    if (!prm.tma_store) mc = mp;   // not read
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = wide ? launch<256, kGrouped>(mp, mq, mp, prm, device_sm_count(), st)
-                         : launch<128, kGrouped>(mp, mq, mp, prm, device_sm_count(), st);
+    cudaError_t e = wide ? launch<256, kGrouped>(mp, mq, mc, prm, device_sm_count(), st)
+                         : launch<128, kGrouped>(mp, mq, mc, prm, device_sm_count(), st);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -154,3 +154,32 @@ def test_moe_chain_config_shapes_sampled(fp8):
     y, ymag = oracle.moe_combine(host_bits(o2), rt.weights, o_pr, tokens=tokens)
     yf_h = host_f32(yf)[tokens].astype(np.float64)
     assert np.all(np.abs(yf_h - y) <= topk * 2.0 ** -24 * ymag + 1e-30)
+
+
+@pytest.mark.parametrize("N", [512, 384])
+def test_grouped_bf16_only_tile_store(fp8, N):
+    # bf16-only output leaves through 16-row TMA boxes (128x256 tiles for
+    # N = 512, 128x128 for 384); an expert's rows ending inside a 16-row half
+    # are stored directly.  Bit-identical to the direct stores of a call that
+    # also asks for fp32; rows past the last expert keep their sentinel
+    counts = [1, 15, 16, 17, 31, 32, 33, 135, 0, 160, 7]
+    G, K = len(counts), 256
+    offsets = np.zeros(G + 1, np.int32)
+    offsets[1:] = np.cumsum(counts)
+    R = int(offsets[-1]) + 24
+    a = syn.random_e4m3_codes((R, K), 21)
+    as_ = syn.random_scales((R, K // 128), 22)
+    b = syn.random_e4m3_codes((G, N, K), 23)
+    bs = syn.random_scales((G, N // 128, K // 128), 24)
+    args = (dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs), dev_i32(offsets))
+    sentinel = 0x7FBF
+    buf = torch.full((R, N), sentinel, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    fp8.fp8_grouped_gemm(*args, c_bf16=buf)
+    cb, cf = fp8.fp8_grouped_gemm(*args, out_bf16=True, out_fp32=True)
+    fp8.fp8_device_status()
+    got, ref_b = host_bits(buf), host_bits(cb)
+    n = int(offsets[-1])
+    assert np.all(got[n:] == sentinel), "rows past the last expert were written"
+    assert np.array_equal(got[:n], ref_b[:n]), "TMA-stored bf16 differs from direct stores"
+    ref, mag = oracle.grouped_gemm(a, as_, b, bs, offsets)
+    check_gemm(ref, mag, host_f32(cf)[:n], got[:n], f"grouped bf16-only N={N}")
