@@ -364,6 +364,17 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster,
+// counted as 16 transaction bytes on that CTA's mbarrier remote_bar: the
+// receiver's barrier completes once every such store has landed, with no
+// fence or arrive on the sender's side.
+__device__ __forceinline__ void st_async_f4(uint32_t remote_saddr, float4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_saddr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_acq_rel_cluster() {
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }

@@ -599,7 +599,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         }
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
-        mbar_init(red_bar, p.ksplit > 1 ? p.ksplit : 1);
+        mbar_init(red_bar, 1);   // cluster split-K: the owner's own arrival + the pushed bytes
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -899,22 +899,22 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             if constexpr (is_swap<V>()) {
                 if (p.ksplit > 1) {
                     // ---- cluster split-K: every CTA pushes each tile row of its
-                    // partial to the CTA that owns that row (rank = row / rows);
-                    // the owner reduces the c partials in rank order
+                    // partial to the CTA that owns that row (rank = row / rows)
+                    // with asynchronous remote stores that count as transaction
+                    // bytes on the owner's barrier; the owner, expecting
+                    // 128 x BN x 4 bytes, reduces the c partials in rank order
                     const int c = p.ksplit, rows = 128 / c;
                     const uint32_t rank = cluster_rank();
                     {
                         const uint32_t owner = static_cast<uint32_t>(e / rows);
                         const uint32_t dst = cluster_map(
                             smem_u32(s_recv + (static_cast<int>(rank) * rows + e % rows) * BN), owner);
+                        const uint32_t bar = cluster_map(smem_u32(red_bar), owner);
 #pragma unroll
                         for (int j = 0; j < BN; j += 4)
-                            st_cluster_f4(dst + j * 4, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
+                            st_async_f4(dst + j * 4, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]), bar);
                     }
-                    if (!(ok = epi_sync(epi_bar, epi_phase, abort_flag))) break;
-                    // lane r of the first epilogue warp tells owner r; each release covers
-                    // the pushes of every thread ordered before it by the barrier above
-                    if (e < c) mbar_arrive_remote(cluster_map(smem_u32(red_bar), static_cast<uint32_t>(e)));
+                    if (e == 0) mbar_arrive_expect_tx(red_bar, 128u * BN * 4u);
                     if (!warp_all(mbar_wait(red_bar, 0, abort_flag))) {
                         set_abort(abort_flag);
                         ok = false;
