@@ -4,10 +4,9 @@ Workload of the headline line: DeepSeek-V3 decode-shaped linears at batch
 M=16 tokens -- wq_a (7168->1536), wq_b (1536->24576), wo (16384->7168) --
 with bf16 activations ~N(0,1) (0.5% outliers x30) and e4m3 weights with
 128x128 fp32 block scales drawn from N(0, 0.02).  One step = act_quant +
-fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer:
-wq_a runs as one kernel (the quantisation inside the GEMM), wq_b and wo as
-an act_quant kernel followed by the GEMM kernel -- five launches, replayed
-from CUDA graphs.  Four weight sets (4 x 167 MB) rotate between steps so
+fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer,
+each one kernel at this batch (the quantisation runs inside the GEMM) --
+three launches, replayed from CUDA graphs.  Four weight sets (4 x 167 MB) rotate between steps so
 every step streams its weights from HBM (inputs larger than L2).
 
 value  = algorithmic HBM bytes of the step / device time (GB/s); the
@@ -16,12 +15,12 @@ value  = algorithmic HBM bytes of the step / device time (GB/s); the
 e2e    = same metric through the Python binding with host buffers: each
          step copies the activations host->device, runs the three calls
          and copies the outputs device->host;
-roofline = the dominant kernel, wo's GEMM (the largest share of the step in
-         the ncu launch list): its algorithmic bytes per launch over its
-         per-launch duration, from CUDA events around a graph of its four
-         weight-rotation launches (activations quantised beforehand),
-         replayed right after the timed region; the other layers' GEMM
-         kernels are timed the same way and listed beside it;
+roofline = the dominant kernel, wo's fused linear kernel (the largest share
+         of the step in the ncu launch list): its algorithmic bytes per
+         launch over its per-launch duration, from CUDA events around a
+         graph of its four weight-rotation launches, replayed right after
+         the timed region; the other layers' kernels are timed the same way
+         and listed beside it;
 cpu_baseline = the CPU oracle on the host cores over a bounded sample.
 
 With --impl reference the CPU oracle itself is timed on the same workload
@@ -515,6 +514,8 @@ def _ncu_dequant(fp8, torch):
 NCU_CASES = {
     "decode_wo": lambda fp8, torch: _ncu_gemm(fp8, torch, 16, *syn.DECODE_LAYERS["wo"]),
     "decode_wq_a_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wq_a"]),
+    "decode_wq_b_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wq_b"]),
+    "decode_wo_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wo"]),
     "prefill_w13": lambda fp8, torch: _ncu_gemm(fp8, torch, 4096, 2 * syn.MLP_INTER, syn.MLP_DIM),
     "act_quant": _ncu_act_quant,
     "weight_dequant": _ncu_dequant,
@@ -599,22 +600,23 @@ def main():
     ms = t_start.elapsed_time(t_end)
     fp8.fp8_device_status()
 
-    # per-launch durations of each layer's GEMM kernel: a graph of its
-    # launches over the four weight rotations (activations quantised
-    # beforehand), events around 50 replays
+    # per-launch durations of each layer's linear (one kernel at this batch;
+    # else act_quant + GEMM): a graph of its launches over the four weight
+    # rotations, events around 50 replays
     per_layer = {}
     launches_per_step = 0
+    fused = {}
     for name in LAYERS:
         N, K = syn.DECODE_LAYERS[name]
-        launches_per_step += 1 if int(fp8.lib.fp8_linear_workspace_size(M, N, K)) == 0 else 2
+        fused[name] = int(fp8.lib.fp8_linear_workspace_size(M, N, K)) == 0
+        launches_per_step += 1 if fused[name] else 2
         if args.no_layer_timing:
             continue
-        xq = [fp8.fp8_act_quant(dec.x[r][name]) for r in range(dec.R)]
 
-        def gemms(name=name, xq=xq):
+        def gemms(name=name):
             for r in range(dec.R):
                 wq, wsc = dec.w[r][name]
-                fp8.fp8_gemm(xq[r][0], xq[r][1], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
+                fp8.fp8_linear(dec.x[r][name], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
         g = capture(torch, gemms)
         per_layer[name] = time_graph(torch, g, 50) / dec.R
         del g
@@ -672,8 +674,8 @@ def main():
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out", "data": "synthetic",
         "config": {"workload": "decode linears wq_a 7168->1536, wq_b 1536->24576, wo 16384->7168; "
-                               "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear: one fused kernel "
-                               "for wq_a, act_quant + GEMM kernels for wq_b and wo)",
+                               "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear: one kernel per "
+                               "layer, the quantisation inside the GEMM)",
                    "global_batch": M * world, "parallelism": f"replicas x{world}",
                    "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
                    "launch": "CUDA graph per step"},
@@ -685,18 +687,20 @@ def main():
     }
     if have_ev:
         N, K = syn.DECODE_LAYERS[dom]
-        achieved = gemm_bytes(M, N, K) / per_layer[dom] / 1e6
-        line["roofline"] = {"kernel": f"fp8_gemm {dom} ({N}x{K}, M={M}): swap-AB cluster split-K GEMM",
+        achieved = linear_bytes(M, N, K) / per_layer[dom] / 1e6
+        what = ("act_quant fused into the swap-AB cluster split-K GEMM" if fused[dom]
+                else "act_quant kernel + swap-AB GEMM kernel")
+        line["roofline"] = {"kernel": f"fp8_linear {dom} ({N}x{K}, M={M}): {what}",
                             "bound": "hbm", "achieved": achieved,
                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                             "peak_kind": f"{peak_src} copy bandwidth (burst)",
-                            "traffic": profiled_traffic("fp8_gemm", f"{dom}_M{M}"),
-                            "algorithmic_bytes_per_launch": gemm_bytes(M, N, K),
+                            "traffic": profiled_traffic("fp8_linear", f"{dom}_M{M}") if fused[dom] else None,
+                            "algorithmic_bytes_per_launch": linear_bytes(M, N, K),
                             "launch_us": per_layer[dom] * 1e3,
-                            "gemm_launch_us": {n: v * 1e3 for n, v in per_layer.items()},
-                            "gemm_GBps": {n: gemm_bytes(M, *syn.DECODE_LAYERS[n]) / v / 1e6
-                                          for n, v in per_layer.items()},
-                            "timing": "per layer: CUDA graph of its 4 weight-rotation GEMM launches, "
+                            "layer_launch_us": {n: v * 1e3 for n, v in per_layer.items()},
+                            "layer_GBps": {n: linear_bytes(M, *syn.DECODE_LAYERS[n]) / v / 1e6
+                                           for n, v in per_layer.items()},
+                            "timing": "per layer: CUDA graph of its 4 weight-rotation fp8_linear launches, "
                                       "events around 50 replays, right after the timed region"}
     if rank == 0 and world == 1 and not args.no_cpu:
         secs, nb, fl = oracle_decode_sample(torch, dec, 16)

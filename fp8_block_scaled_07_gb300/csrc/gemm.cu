@@ -139,7 +139,9 @@ struct Cfg {
     // 128x256 tiles: 8 epilogue warps, two per TMEM lane quarter, each owning
     // 128 of the 256 columns; their warpgroups take registers from warps 0-3
     static constexpr int kEpiWarps = BN == 256 ? 8 : 4;
-    static constexpr int kThreads = 128 + 32 * kEpiWarps;
+    // fused: two more quantiser warps after the epilogue (four in all)
+    static constexpr int kQuantWarps = kFusedV ? 4 : 0;
+    static constexpr int kThreads = 128 + 32 * kEpiWarps + (kFusedV ? 64 : 0);
     static constexpr int kCPT = BN * 4 / kEpiWarps;   // accumulator columns per epilogue thread
     static constexpr bool kSplitRegs = kEpiWarps == 8;
     // the producer and MMA warps keep their tile state in registers (spills
@@ -402,20 +404,23 @@ __device__ __forceinline__ int store_tile_tma(const CUtensorMap* tm_c, uint8_t* 
     return 32;
 }
 
-// Fused act_quant for the swapped decode layout (BN == 16, 64 threads):
-// thread (r, sub) quantises values [32 sub, 32 sub + 32) of token row r of
-// each slab from the bf16 tile TMA placed in shared memory (two 64-column
-// halves, 128-byte swizzle); the four threads of a row share the block max
-// by shuffles.  Codes go to the stage's e4m3 tile in the layout the MMA
-// reads; the scale products b_s * a_s go to a ring the epilogue reads.
+// Fused act_quant for the swapped decode layout (BN == 16): four quantiser
+// warps (2-3 and the two after the epilogue warps), 128 threads; thread
+// (r, sub) quantises values [16 sub, 16 sub + 16) of token row r of each
+// slab from the bf16 tile TMA placed in shared memory (two 64-column halves,
+// 128-byte swizzle); the eight threads of a row share the block max by
+// shuffles.  Codes go to the stage's e4m3 tile in the layout the MMA reads;
+// the scale products b_s * a_s go to a ring the epilogue reads.
 template <int BN, int S>
 __device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, const int* s_prefix, uint8_t* sQ,
                                                const uint8_t* sX, float* s_ring, uint64_t* full, uint64_t* xfull,
                                                volatile int* abort_flag) {
     static_assert(BN == 16, "fused quantisation covers 16-token tiles");
     constexpr int kQTile = BN * kBlock, kXTile = BN * kBlock * 2, kRing = S + 2;
-    const int qt = threadIdx.x - 64, lane = threadIdx.x & 31;
-    const int r = qt >> 2, sub = qt & 3;
+    const int t = static_cast<int>(threadIdx.x);
+    const int qt = t < 128 ? t - 64 : t - 256 + 64;   // 0..127 over warps 2-3, 8-9
+    const int lane = t & 31;
+    const int r = qt >> 3, sub = qt & 7;
     uint32_t iter = 0;
     Seg sg;
     while (it.next(sg)) {
@@ -430,27 +435,28 @@ __device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, cons
                 set_abort(abort_flag);
                 return;
             }
-            const uint8_t* xrow = sX + st * kXTile + (sub >> 1) * (kXTile / 2) + r * 128;
-            float f[4][8];
+            // columns [16 sub, 16 sub + 16): half sub / 4, chunks 2 (sub % 4) and +1
+            const uint8_t* xrow = sX + st * kXTile + (sub >> 2) * (kXTile / 2) + r * 128;
+            float f[2][8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = (sub & 1) * 4 + i;
+            for (int i = 0; i < 2; ++i) {
+                const int c = (sub & 3) * 2 + i;
                 unpack_bf16x8(*reinterpret_cast<const uint4*>(xrow + ((c ^ (r & 7)) * 16)), f[i]);
             }
-            float amax = fmaxf(fmaxf(max_abs8(f[0]), max_abs8(f[1])), fmaxf(max_abs8(f[2]), max_abs8(f[3])));
+            float amax = fmaxf(max_abs8(f[0]), max_abs8(f[1]));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
             const float sc = block_scale(amax, p.ue8m0 != 0);
-            uint2 q[4];
+            uint2 q[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 q[i] = p.ue8m0 ? quant8<true>(f[i], sc) : quant8<false>(f[i], sc);
                 if (!valid) q[i] = make_uint2(0, 0);
             }
-            // 16-byte e4m3 chunks 2*sub and 2*sub+1 of row r, 128-byte swizzle
+            // 16-byte e4m3 chunk sub of row r, 128-byte swizzle
             uint8_t* row = sQ + st * kQTile + r * 128;
-            *reinterpret_cast<uint4*>(row + (((2 * sub) ^ (r & 7)) * 16)) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
-            *reinterpret_cast<uint4*>(row + (((2 * sub + 1) ^ (r & 7)) * 16)) = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
+            *reinterpret_cast<uint4*>(row + ((sub ^ (r & 7)) * 16)) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
             if (sub == 0) s_ring[(iter % kRing) * BN + r] = valid ? bsc * sc : 0.0f;
             fence_proxy_async_smem();
             __syncwarp();
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], C::kFused ? 3 : 1);   // fused: TMA + two quantiser warps
+            mbar_init(&full[i], C::kFused ? 1 + C::kQuantWarps : 1);   // fused: TMA + the quantiser warps
             mbar_init(&empty[i], 1);
             if (C::kFused) mbar_init(&xfull[i], 1);
         }
@@ -744,10 +750,12 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         }
     } else if (C::kFused) {
         // ---------------------------------------------------------- quantiser
-        // warps 2-3: act_quant of the token rows of each slab, written as the
-        // e4m3 Q tile in the 128-byte-swizzled layout the MMA reads
+        // warps 2-3 (and 8-9): act_quant of the token rows of each slab,
+        // written as the e4m3 Q tile in the 128-byte-swizzled layout the MMA reads
         if constexpr (C::kFused) quantiser_role<BN, S>(p, it, s_prefix, sQ, sX, s_ring, full, xfull, abort_flag);
     }
+    } else if (C::kFused && warp >= kEpiWarp0 + C::kEpiWarps) {
+        if constexpr (C::kFused) quantiser_role<BN, S>(p, it, s_prefix, sQ, sX, s_ring, full, xfull, abort_flag);
     } else {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
         // ---------------------------------------------------------- epilogue
@@ -950,9 +958,10 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     continue;
                 }
             }
-            // ---- stream-K fixup (dense only): partial tile.  The 128x256
-            // kernels only ever run whole tiles (the host plans them so).
-            if constexpr (C::kSplitRegs) {
+            // ---- stream-K fixup: partial tile.  The 128x256 kernels only
+            // ever run whole tiles and the fused kernel only cluster split-K
+            // (the host plans them so); compiled out of both.
+            if constexpr (C::kSplitRegs || C::kFused) {   // never planned for these
                 set_abort(abort_flag);
                 ok = false;
                 break;
@@ -1394,12 +1403,13 @@ extern "C" fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const vo
 namespace {
 constexpr size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// The fused kernel saves the act_quant launch (~3 us on GB300) but every CTA
-// quantises its own slabs, redundantly across output tiles (~0.2-0.3 us per
-// slab on two warps): it is used when a CTA's K range is short.  Measured at
-// M=16: wq_a (7 slabs per CTA) 8.5 vs 9.0 us, wq_b (12) 12.8 vs 11.8 us,
-// wo (32) 28.9 vs 24.7 us for fused vs act_quant + fp8_gemm.
-constexpr int kFusedMaxSlabsPerCta = 8;
+// The fused kernel saves the act_quant launch and its dependency hop, but
+// every CTA quantises its own slabs (redundantly across output tiles) on
+// four warps, which must keep pace with the weight stream.  Measured at M=16
+// on GB300, whole decode step (wq_a, wq_b, wo): 50.0 us with only wq_a (7
+// slabs per CTA) fused, 49.3 us with all three (wo: 32 slabs per CTA)
+// fused; longer K ranges per CTA are not measured and stay staged.
+constexpr int kFusedMaxSlabsPerCta = 64;
 
 bool linear_is_fused(int64_t M, int64_t N, int64_t K) {
     if (M > 16) return false;

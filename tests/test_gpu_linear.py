@@ -43,10 +43,16 @@ def _compare(fp8, x_bits, w_bits, ue8m0, what, expect_fused=None):
 
 @pytest.mark.parametrize("M", [1, 5, 16])
 def test_decode_linears(fp8, M):
-    # wq_a splits K into short ranges per CTA (fused kernel); wq_b and wo
-    # stage the quantised activations in the workspace
+    # every decode layer at M <= 16 runs the fused kernel (7, 12 and 32 slabs
+    # per CTA for wq_a, wq_b and wo)
     for lin in syn.decode_linears(M):
-        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M={M}", expect_fused=(lin.name == "wq_a"))
+        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M={M}", expect_fused=True)
+
+
+def test_decode_linears_staged_above_16_tokens(fp8):
+    # M = 33: act_quant into the workspace, then fp8_gemm
+    for lin in syn.decode_linears(33):
+        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M=33", expect_fused=False)
 
 
 def test_fused_ue8m0_ragged_n(fp8):
