@@ -74,13 +74,22 @@ lib = _load()
 
 
 # ------------------------------------------------------------------ helpers
+# (kept light: a decode-sized call spends more time here than in the C entry)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    return t.data_ptr() if t is not None else None   # c_void_p arguments take ints
 
 
-def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+def _stream(stream=None, device=None):
+    """Raw cudaStream_t of `stream`, else of the current stream of `device`
+    (an index; the current device if None)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device() if device is None else device)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check(name, status):
@@ -89,15 +98,16 @@ def _check(name, status):
 
 
 def _cuda(t, name, dtypes, ndim=None):
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype in dtypes and t.is_contiguous()
+            and (ndim is None or t.dim() == ndim)):
+        return t
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if ndim is not None and t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
-    return t
+    raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
 _E4M3 = (torch.float8_e4m3fn, torch.uint8)
@@ -153,13 +163,17 @@ class _Workspace:
         self._lock = threading.Lock()
 
     def get(self, nbytes, device, stream):
+        """device: CUDA device index; stream: raw cudaStream_t of the call."""
         if nbytes == 0:
             return None
-        key = (device.index, stream.cuda_stream)
+        key = (device, stream)
+        buf = self._bufs.get(key)
+        if buf is not None and buf.numel() >= nbytes:
+            return buf
         with self._lock:
             buf = self._bufs.get(key)
             if buf is None or buf.numel() < nbytes:
-                buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+                buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=torch.device("cuda", device))
                 self._bufs[key] = buf
             return buf
 
@@ -170,6 +184,20 @@ class _Workspace:
 
 
 workspaces = _Workspace()
+
+
+_ws_sizes = {}
+
+
+def _ws_size(fn, M, N, K, device):
+    """Workspace bytes of a call on `device` (an index), cached per shape: the
+    plan depends only on the shape and the device's SM count."""
+    key = (fn, M, N, K, device)
+    v = _ws_sizes.get(key)
+    if v is None:
+        with torch.cuda.device(device):
+            v = _ws_sizes[key] = int(getattr(lib, fn)(M, N, K))
+    return v
 
 
 def fp8_gemm_workspace_size(M, N, K):
@@ -193,12 +221,13 @@ def fp8_gemm(a, a_s, b, b_s, out_bf16=True, out_fp32=False, c_bf16=None, c_fp32=
         c_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     if c_fp32 is None and out_fp32:
         c_fp32 = torch.empty((M, N), dtype=torch.float32, device=a.device)
-    st = torch.cuda.current_stream() if stream is None else stream
+    st = _stream(stream)
     if workspace is None:
-        workspace = workspaces.get(fp8_gemm_workspace_size(M, N, K), a.device, st)
+        dev = a.get_device()
+        workspace = workspaces.get(_ws_size("fp8_gemm_workspace_size", M, N, K, dev), dev, st)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("fp8_gemm", lib.fp8_gemm(_ptr(a), _ptr(a_s), _ptr(b), _ptr(b_s), _ptr(c_bf16), _ptr(c_fp32),
-                                    M, N, K, _ptr(workspace), ws_bytes, _stream(st)))
+                                    M, N, K, _ptr(workspace), ws_bytes, st))
     return c_bf16, c_fp32
 
 
@@ -302,10 +331,11 @@ def fp8_linear(x, w, w_s, scale_fmt=FP8_SCALE_FP32, out_bf16=True, out_fp32=Fals
         c_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if c_fp32 is None and out_fp32:
         c_fp32 = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    st = torch.cuda.current_stream() if stream is None else stream
+    st = _stream(stream)
     if workspace is None:
-        workspace = workspaces.get(int(lib.fp8_linear_workspace_size(M, N, K)), x.device, st)
+        dev = x.get_device()
+        workspace = workspaces.get(_ws_size("fp8_linear_workspace_size", M, N, K, dev), dev, st)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("fp8_linear", lib.fp8_linear(_ptr(x), _ptr(w), _ptr(w_s), _ptr(c_bf16), _ptr(c_fp32), M, N, K,
-                                        int(scale_fmt), _ptr(workspace), ws_bytes, _stream(st)))
+                                        int(scale_fmt), _ptr(workspace), ws_bytes, st))
     return c_bf16, c_fp32
