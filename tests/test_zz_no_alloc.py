@@ -75,8 +75,9 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(fp8):
 
 
 def test_shapes_needing_more_scratch_are_rejected(fp8):
-    # 64 tokens x 192 output tiles: stream-K partials of ~10 MB on 152 SMs
-    M, N, K = 64, 24576, 1536
+    # 64 output tiles of 128 x 128 over K = 8192: stream-K partials of
+    # ~20 MB on 152 SMs
+    M, N, K = 1024, 1024, 8192
     if fp8.fp8_gemm_workspace_size(M, N, K) <= SCRATCH_BYTES:
         pytest.skip("this device's schedule fits the fixed scratch")
     a = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
