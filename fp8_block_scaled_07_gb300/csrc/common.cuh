@@ -108,29 +108,52 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
 // a bf16 value and s = RN(max(|x|max, 1e-4) / 448) of its block, so x/s
 // depends only on the two 8-bit mantissas and their exponent gap; the
 // parity tests enumerate that whole domain against the oracle's IEEE
-// division.  A zero x keeps its sign.
+// division.  The remainder is formed negated, e' = q0 s - x, and q = RN(q0 -
+// e' r): the same roundings (nearest-even is symmetric), and a zero x keeps
+// its sign with no test, as every sum of zeros then rounds to the sign of x.
+// The core takes the negated values nx = -x and -r, so that every step is a
+// packed two-lane multiply or fma with no negated operand: q0 = RN(nx (-r)),
+// e' = RN(q0 s + nx), q = RN(e' (-r) + q0).
 template <bool UE8M0>
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
-    float q[8];
-    const float r = __frcp_rn(s);
-    if (UE8M0) {
+__device__ __forceinline__ uint2 quant8n(const float (&nx)[8], float s, float r) {
+    const float2 nr2 = make_float2(-r, -r), s2 = make_float2(s, s);
+    float2 q[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(f[i], r);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float q0 = __fmul_rn(f[i], r);
-            const float e = __fmaf_rn(-q0, s, f[i]);
-            const float q1 = __fmaf_rn(e, r, q0);
-            q[i] = f[i] == 0.0f ? f[i] : q1;
+    for (int i = 0; i < 4; ++i) {
+        const float2 n2 = make_float2(nx[2 * i], nx[2 * i + 1]);
+        const float2 q0 = __fmul2_rn(n2, nr2);
+        if (UE8M0) {
+            q[i] = q0;   // s is a power of two: x (1/s) is exact
+        } else {
+            const float2 en = __ffma2_rn(q0, s2, n2);
+            q[i] = __ffma2_rn(en, nr2, q0);
         }
     }
     uint2 out;
-    out.x = static_cast<uint32_t>(f32x2_to_e4m3x2(q[0], q[1])) |
-            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[2], q[3])) << 16);
-    out.y = static_cast<uint32_t>(f32x2_to_e4m3x2(q[4], q[5])) |
-            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[6], q[7])) << 16);
+    out.x = static_cast<uint32_t>(f32x2_to_e4m3x2(q[0].x, q[0].y)) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[1].x, q[1].y)) << 16);
+    out.y = static_cast<uint32_t>(f32x2_to_e4m3x2(q[2].x, q[2].y)) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[3].x, q[3].y)) << 16);
     return out;
+}
+
+template <bool UE8M0>
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+    float nx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) nx[i] = -f[i];
+    return quant8n<UE8M0>(nx, s, __frcp_rn(s));
+}
+
+// 8 bf16 (one 16-byte load) -> their 8 negated fp32 values, exact (the sign
+// bit flipped), for quant8n.
+__device__ __forceinline__ void unpack_bf16x8_neg(const uint4& v, float (&nx)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        nx[2 * i] = __uint_as_float((w[i] << 16) ^ 0x80000000u);
+        nx[2 * i + 1] = __uint_as_float((w[i] & 0xFFFF0000u) ^ 0x80000000u);
+    }
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the

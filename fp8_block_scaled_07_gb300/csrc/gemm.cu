@@ -437,21 +437,22 @@ __device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, cons
             }
             // columns [16 sub, 16 sub + 16): half sub / 4, chunks 2 (sub % 4) and +1
             const uint8_t* xrow = sX + st * kXTile + (sub >> 2) * (kXTile / 2) + r * 128;
-            float f[2][8];
+            float nx[2][8];   // the values negated, as quant8n takes them
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int c = (sub & 3) * 2 + i;
-                unpack_bf16x8(*reinterpret_cast<const uint4*>(xrow + ((c ^ (r & 7)) * 16)), f[i]);
+                unpack_bf16x8_neg(*reinterpret_cast<const uint4*>(xrow + ((c ^ (r & 7)) * 16)), nx[i]);
             }
-            float amax = fmaxf(max_abs8(f[0]), max_abs8(f[1]));
+            float amax = fmaxf(max_abs8(nx[0]), max_abs8(nx[1]));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
             const float sc = block_scale(amax, p.ue8m0 != 0);
+            const float rc = __frcp_rn(sc);
             uint2 q[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                q[i] = p.ue8m0 ? quant8<true>(f[i], sc) : quant8<false>(f[i], sc);
+                q[i] = p.ue8m0 ? quant8n<true>(nx[i], sc, rc) : quant8n<false>(nx[i], sc, rc);
                 if (!valid) q[i] = make_uint2(0, 0);
             }
             // 16-byte e4m3 chunk sub of row r, 128-byte swizzle
