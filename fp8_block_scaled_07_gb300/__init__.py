@@ -44,6 +44,7 @@ def _declare(lib):
         "fp8_weight_dequant": (st, [vp, f32p, vp, i64, i64, vp]),
         "fp8_gemm_workspace_size": (sz, [i64, i64, i64]),
         "fp8_gemm": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, vp, sz, vp]),
+        "fp8_gemm_ue8m0": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, vp]),
         "fp8_grouped_gemm": (st, [vp, f32p, vp, f32p, vp, i32, i64, vp, f32p, i64, i64, vp]),
         "fp8_silu_mul_quant": (st, [vp, vp, i64, i64, i64, vp, f32p, vp, ctypes.c_int, vp]),
         "fp8_moe_route": (st, [vp, i64, i32, i32, vp, vp, vp, vp]),
@@ -228,6 +229,28 @@ def fp8_gemm(a, a_s, b, b_s, out_bf16=True, out_fp32=False, c_bf16=None, c_fp32=
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("fp8_gemm", lib.fp8_gemm(_ptr(a), _ptr(a_s), _ptr(b), _ptr(b_s), _ptr(c_bf16), _ptr(c_fp32),
                                     M, N, K, _ptr(workspace), ws_bytes, st))
+    return c_bf16, c_fp32
+
+
+def fp8_gemm_ue8m0(a, a_s, b, b_s, out_bf16=True, out_fp32=False, c_bf16=None, c_fp32=None, stream=None):
+    """fp8_gemm for power-of-two (ue8m0) scales on the tensor core's block-scaled
+    MMA.  Returns (c_bf16 or None, c_fp32 or None)."""
+    _cuda(a, "a", _E4M3, 2)
+    _cuda(b, "b", _E4M3, 2)
+    _cuda(a_s, "a_s", _F32, 2)
+    _cuda(b_s, "b_s", _F32, 2)
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("K mismatch")
+    if tuple(a_s.shape) != (M, K // BLOCK) or tuple(b_s.shape) != ((N + BLOCK - 1) // BLOCK, K // BLOCK):
+        raise ValueError("scale shape mismatch")
+    if c_bf16 is None and out_bf16:
+        c_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if c_fp32 is None and out_fp32:
+        c_fp32 = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check("fp8_gemm_ue8m0", lib.fp8_gemm_ue8m0(_ptr(a), _ptr(a_s), _ptr(b), _ptr(b_s), _ptr(c_bf16),
+                                                _ptr(c_fp32), M, N, K, _stream(stream)))
     return c_bf16, c_fp32
 
 

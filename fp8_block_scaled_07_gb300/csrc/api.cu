@@ -38,7 +38,7 @@ extern "C" fp8_status fp8_device_status(void* stream) {
 extern "C" const char* fp8_status_string(fp8_status status) {
     switch (status) {
         case FP8_OK: return "ok";
-        case FP8_ERR_INVALID_ARG: return "invalid argument (pointer, size or alignment)";
+        case FP8_ERR_INVALID_ARG: return "invalid argument (pointer, size, alignment, or a ue8m0 scale that is not a power of two)";
         case FP8_ERR_UNSUPPORTED: return "unsupported shape";
         case FP8_ERR_CUDA: return "CUDA error";
         case FP8_ERR_TIMEOUT: return "a kernel's bounded wait timed out";

@@ -322,6 +322,50 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// Instruction descriptor for the block-scaled kind (mxf8f6f4 with E8M0
+// scales, one per 32 K values of each A row and each B column): D f32 is
+// implied; A and B e4m3, K-major, shape M x N; sf_id picks the byte of each
+// 32-bit scale word in tensor memory (the K=32 step within a 128-K slab).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4)                // B scale byte
+         | (0u << 7) | (0u << 10)                             // A, B: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (1u << 23)                                         // scales are E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)
+         | (static_cast<uint32_t>(sf_id) << 29);              // A scale byte
+}
+
+// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb)^T, one K=32 step of e4m3 with E8M0
+// block scales read from tensor memory: the scale of A row m at lane m,
+// column sfa + m/32; the scale of B column n at column sfb + n/32, lane
+// n % 32 of every lane quarter (rows of quarter q read quarter q's copy).
+__device__ __forceinline__ void mma_mx_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 bit stores into tensor memory: thread i of the warp writes
+// columns [col, col + 4) (x4) or [col, col + 8) (x8) of lane (lane_base + i).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t a, uint32_t b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %1, %1, %1, %2, %2, %2, %2};" ::"r"(taddr),
+                 "r"(a), "r"(b)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {

@@ -1053,6 +1053,273 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     if (threadIdx.x == 0) FP8BS_TRACE(7);
 }
 
+// ------------------------------------------------------------------ ue8m0: block-scaled MMA
+// When every scale is a power of two (scale_fmt ue8m0) the tensor core can
+// apply the block scales itself: tcgen05.mma kind::mxf8f6f4 with one E8M0
+// scale per 32 K values of each A row and each B column, read from tensor
+// memory.  A 128-K block's scale is that scale for all four of its K=32
+// steps.  A tile then accumulates over the whole of K in TMEM and its
+// epilogue runs once, instead of promoting every 128-K slab in registers.
+//
+// 128x256 tiles, whole tiles per persistent CTA (m-fastest, as the dense
+// kernel).  Warp 0: TMA producer; warp 1: MMA issuer; warps 2-5 (one per
+// TMEM lane quarter): write each slab's scale factors into a ring of TMEM
+// slots kMxSfSlots slabs ahead of the MMA, and run each tile's epilogue.
+// TMEM: the accumulator in columns [0, 256), scale slot s at 256 + 16 s
+// (A's scales in its first 4 columns, B's in the next 8).
+constexpr int kMxBN = 256;
+constexpr int kMxStages = 4;
+constexpr int kMxSfSlots = 8;
+constexpr int kMxThreads = 192;
+constexpr int kMxSfCol0 = 256;
+constexpr int kMxStageBytes = kPTileBytes + kMxBN * kBlock;   // A 16 KB + B 32 KB
+constexpr int kMxStgBytes = 4 * 32 * 128;                     // per epilogue warp a 32 x 64 bf16 box
+constexpr int kMxSmemBytes = 1024 + kMxStages * kMxStageBytes + kMxStgBytes + 1024;
+
+// E8M0 code of a power-of-two fp32 scale (its biased exponent); `bad` is set
+// for anything else (a mantissa, a sign, zero, a subnormal, inf or NaN).
+__device__ __forceinline__ uint32_t e8m0_code(float s, bool& bad) {
+    const uint32_t u = __float_as_uint(s);
+    const uint32_t e = u >> 23;   // sign bit included: negative values land above 255
+    bad |= (u & 0x7FFFFFu) != 0u || e == 0u || e >= 255u;
+    return e & 0xFFu;
+}
+
+__global__ void __launch_bounds__(kMxThreads, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_c, const Params p) {
+    constexpr int S = kMxStages, R = kMxSfSlots;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;                                    // S x 16 KB
+    uint8_t* sB = smem + S * kPTileBytes;                  // S x 32 KB
+    uint8_t* sStg = smem + S * kMxStageBytes;              // 4 x 4 KB output staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + kMxStgBytes);
+    uint64_t* full = bars;                      // S: operand tiles landed
+    uint64_t* empty = bars + S;                 // S: the MMAs have read them
+    uint64_t* sf_full = bars + 2 * S;           // R: scale slot written (4 warps)
+    uint64_t* sf_empty = bars + 2 * S + R;      // R: the MMAs that read it are done
+    uint64_t* acc_full = bars + 2 * S + 2 * R;  // tile accumulated
+    uint64_t* acc_empty = acc_full + 1;         // accumulator read out (4 warps)
+    uint64_t* mma_done = acc_full + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&sf_full[i], 4);
+            mbar_init(&sf_empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        if (p.tma_store) tma_prefetch_desc(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    if (threadIdx.x == 64) griddep_launch_dependents();
+    griddep_wait();
+
+    // this CTA's tiles: blockIdx.x + i * gridDim.x
+    const int my_tiles = static_cast<int>(blockIdx.x) < p.num_tiles
+                             ? (p.num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                   static_cast<int>(gridDim.x)
+                             : 0;
+    const uint32_t KB = static_cast<uint32_t>(p.KB);
+    const uint32_t total = static_cast<uint32_t>(my_tiles) * KB;
+    auto tile_of = [&](int ord) {
+        return tile_geom<kMxBN, kDense>(p, static_cast<int>(blockIdx.x) + ord * static_cast<int>(gridDim.x),
+                                        nullptr);
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t iter = 0;
+            for (int ord = 0; ord < my_tiles && iter == static_cast<uint32_t>(ord) * KB; ++ord) {
+                const Tile tg = tile_of(ord);
+                for (uint32_t kb = 0; kb < KB; ++kb, ++iter) {
+                    const int st = static_cast<int>(iter % S);
+                    if (!mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag)) {
+                        set_abort(abort_flag);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], kMxStageBytes);
+                    tma_load_2d(sA + st * kPTileBytes, &tm_a, &full[st], static_cast<int>(kb) * kBlock, tg.p_row0);
+                    tma_load_2d(sB + st * (kMxBN * kBlock), &tm_b, &full[st], static_cast<int>(kb) * kBlock,
+                                tg.q_row0);
+                }
+            }
+            // every load issued must land before the CTA may exit
+            const volatile int never = 0;
+            for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
+                const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
+                if (!mbar_wait(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t iter = 0;
+            bool ok = true;
+            for (int ord = 0; ok && ord < my_tiles; ++ord) {
+                if (!mbar_wait(acc_empty, (static_cast<uint32_t>(ord) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (uint32_t kb = 0; kb < KB; ++kb, ++iter) {
+                    const int st = static_cast<int>(iter % S), r = static_cast<int>(iter % R);
+                    if (!mbar_wait(&full[st], (iter / S) & 1, abort_flag) ||
+                        !mbar_wait(&sf_full[r], (iter / R) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = smem_desc_sw128(smem_u32(sA + st * kPTileBytes));
+                    const uint64_t db = smem_desc_sw128(smem_u32(sB + st * (kMxBN * kBlock)));
+                    const uint32_t sfa = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * r);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)   // 4 x K=32, each with its byte of the scale words
+                        mma_mx_e4m3(tmem_base, da + 2 * kk, db + 2 * kk, idesc_mx_e4m3(128, kMxBN, kk), sfa, sfa + 4,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[st]);
+                    mma_commit(&sf_empty[r]);
+                }
+                if (!ok) break;
+                mma_commit(acc_full);
+            }
+            if (!ok) set_abort(abort_flag);
+            mma_commit(mma_done);
+            const volatile int never = 0;
+            if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
+        }
+    } else {
+        // ---------------------------------------------------------- scales + epilogue
+        const int q = warp & 3;                        // TMEM lane quarter
+        const int e = q * 32 + lane;                   // tile row
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        uint8_t* stg = sStg + (warp - 2) * (32 * 128);
+        bool bad = false, ok = true;
+        // scales of 4 slabs at a time (16-byte loads), the next group loaded
+        // while the current one is written
+        float4 ca{}, cb0{}, cb1{}, na{}, nb0{}, nb1{};
+        auto load_group = [&](uint32_t slab, float4& a4, float4& b04, float4& b14) {
+            if (slab >= total) return;
+            const Tile tg = tile_of(static_cast<int>(slab / KB));
+            const uint32_t kb = slab % KB;
+            const int row = tg.p_row0 + min(e, max(tg.p_valid, 1) - 1);   // rows past M repeat a valid one
+            const int nb = tg.q_row0 / 128;
+            a4 = __ldg(reinterpret_cast<const float4*>(p.a_s + static_cast<int64_t>(row) * KB + kb));
+            b04 = __ldg(reinterpret_cast<const float4*>(p.b_s + static_cast<int64_t>(nb) * KB + kb));
+            b14 = __ldg(reinterpret_cast<const float4*>(p.b_s + static_cast<int64_t>(min(nb + 1, p.NB - 1)) * KB + kb));
+        };
+        load_group(0, na, nb0, nb1);
+        uint32_t iter = 0;   // slabs whose scales are written
+        for (int te = 0; ok && te < my_tiles; ++te) {
+            // scales up to kMxSfSlots slabs into the next tile (their slots
+            // were last read by this tile's MMAs, which need nothing more)
+            const uint32_t limit = min(total, static_cast<uint32_t>(te + 1) * KB + min(KB, static_cast<uint32_t>(R)));
+            for (; iter < limit; ++iter) {
+                // KB % 4 == 0: a group of 4 slabs never straddles two tiles
+                if (iter % 4 == 0) {
+                    ca = na;
+                    cb0 = nb0;
+                    cb1 = nb1;
+                    load_group(iter + 4, na, nb0, nb1);
+                }
+                const int j = static_cast<int>(iter % 4);
+                const float sa = j == 0 ? ca.x : j == 1 ? ca.y : j == 2 ? ca.z : ca.w;
+                const float s0 = j == 0 ? cb0.x : j == 1 ? cb0.y : j == 2 ? cb0.z : cb0.w;
+                const float s1 = j == 0 ? cb1.x : j == 1 ? cb1.y : j == 2 ? cb1.z : cb1.w;
+                const uint32_t wa = e8m0_code(sa, bad) * 0x01010101u;
+                const uint32_t w0 = e8m0_code(s0, bad) * 0x01010101u;
+                const uint32_t w1 = e8m0_code(s1, bad) * 0x01010101u;
+                const int r = static_cast<int>(iter % R);
+                if (!warp_all(mbar_wait(&sf_empty[r], ((iter / R) & 1) ^ 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = tmem_base + lane_off + static_cast<uint32_t>(kMxSfCol0 + 16 * r);
+                tmem_st4(col, wa, wa, wa, wa);   // row e's scale in column e/32 (the others unused)
+                tmem_st8(col + 4, w0, w1);        // columns n/32: n < 128 in the first four
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[r]);
+            }
+            if (!ok) break;
+            // epilogue of tile te
+            if (!warp_all(mbar_wait(acc_full, static_cast<uint32_t>(te) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const Tile tg = tile_of(te);
+            const int row0 = tg.p_row0 + q * 32;
+            const int64_t row = tg.p_row0 + e;
+#pragma unroll 1
+            for (int h = 0; h < kMxBN / 64; ++h) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h), r0);
+                tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h + 32), r1);
+                tmem_wait_ld();
+                float acc[64];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    acc[c] = __uint_as_float(r0[c]);
+                    acc[32 + c] = __uint_as_float(r1[c]);
+                }
+                const int col0 = tg.q_row0 + 64 * h;
+                const int cols = min(64, p.N - col0);
+                if (cols <= 0) break;
+                if (p.c_bf16 && p.tma_store) {
+                    store_tile_tma<64, 32>(&tm_c, stg, lane, col0, row0, tg.p_valid - q * 32, cols, acc);
+                } else if (e < tg.p_valid) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        if (c < cols) {
+                            if (p.c_bf16) p.c_bf16[row * p.N + col0 + c] = __float2bfloat16_rn(acc[c]);
+                            if (p.c_fp32) p.c_fp32[row * p.N + col0 + c] = acc[c];
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+        if (!ok) set_abort(abort_flag);
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_INVALID_ARG));
+        if (lane == 0) bulk_wait_all();   // staging boxes read out before shared memory goes
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1305,6 +1572,54 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     } else {
         e = launch<64, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
     }
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" fp8_status fp8_gemm_ue8m0(const void* a, const float* a_s, const void* b, const float* b_s,
+                                     void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K, void* stream) {
+    if (M < 0 || N < 0 || K <= 0 || K % (4 * kBlock) != 0) return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    if (!a || !a_s || !b || !b_s || (!c_bf16 && !c_fp32)) return FP8_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(a_s) || !aligned16(b_s)) return FP8_ERR_INVALID_ARG;
+    if ((c_bf16 && (reinterpret_cast<uintptr_t>(c_bf16) & 1)) ||
+        (c_fp32 && (reinterpret_cast<uintptr_t>(c_fp32) & 3)))
+        return FP8_ERR_INVALID_ARG;
+    if (N % 8 == 0 && ((c_bf16 && !aligned16(c_bf16)) || (c_fp32 && !aligned16(c_fp32))))
+        return FP8_ERR_INVALID_ARG;
+    Params prm{};
+    prm.a_s = a_s;
+    prm.b_s = b_s;
+    prm.c_bf16 = static_cast<__nv_bfloat16*>(c_bf16);
+    prm.c_fp32 = c_fp32;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.KB = static_cast<int>(K / kBlock);
+    prm.NB = static_cast<int>((N + 127) / 128);
+    prm.G = 1;
+    prm.tiles_p = static_cast<int>((M + 127) / 128);
+    prm.tiles_q = static_cast<int>((N + kMxBN - 1) / kMxBN);
+    const int64_t tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
+    if (tiles > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    prm.num_tiles = static_cast<int>(tiles);
+    CUtensorMap ma, mb, mc;
+    if (!make_map(&ma, a, M, K, 128) || !make_map(&mb, b, N, K, kMxBN)) return FP8_ERR_CUDA;
+    prm.tma_store = (c_bf16 && !c_fp32 && N % 8 == 0) ? 1 : 0;
+    if (prm.tma_store && !make_map_bf16(&mc, c_bf16, M, N, 32)) return FP8_ERR_CUDA;
+    if (!prm.tma_store) mc = ma;   // not read
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, device_sm_count()));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        if (cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemBytes) !=
+            cudaSuccess)
+            return FP8_ERR_CUDA;
+        configured[dev] = 1;
+    }
+    const cudaError_t e =
+        launch_pdl_cluster(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmemBytes, st, 1u, ma, mb, mc, prm);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -31,7 +31,8 @@
  *   - Errors are returned, never raised: FP8_ERR_INVALID_ARG for a bad
  *     pointer, size or alignment (nothing is launched), FP8_ERR_CUDA when a
  *     launch fails.  A kernel whose internal wait ran out of time records
- *     FP8_ERR_TIMEOUT, which fp8_device_status reports.
+ *     FP8_ERR_TIMEOUT, and fp8_gemm_ue8m0 given a scale that is not a power
+ *     of two records FP8_ERR_INVALID_ARG; fp8_device_status reports either.
  *   - Pointers to e4m3 or bf16 matrices read by the GEMMs must be 16-byte
  *     aligned; K must be a multiple of 128.
  */
@@ -103,6 +104,20 @@ size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
                     void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* fp8_gemm for power-of-two scales (the pages' optional scale_fmt "ue8m0":
+ * every scale rounded up to a power of two), computed by the tensor core's
+ * block-scaled MMA: each 128-K block's scales a_s[m, kb] and b_s[n/128, kb]
+ * are applied by the MMA as E8M0 exponents, so a tile accumulates over all
+ * of K without per-block promotion.  Same arguments, layouts and result as
+ * fp8_gemm (the fp32 accumulation order differs; the tolerance is the same),
+ * minus the workspace (none is needed).  Requires K % 512 == 0 and 16-byte
+ * aligned a, b, a_s and b_s (else FP8_ERR_INVALID_ARG).  Every a_s and b_s
+ * value must be a positive normal power of two; any other value makes
+ * fp8_device_status report FP8_ERR_INVALID_ARG, and the output is then
+ * unspecified.  Meant for prefill shapes (128 x 256 output tiles). */
+fp8_status fp8_gemm_ue8m0(const void* a, const float* a_s, const void* b, const float* b_s,
+                          void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K, void* stream);
 
 /* The FP8 branch of the model's linear() (source tour, "FP8 with per-block
  * scales": act_quant of the activations, then fp8_gemm against the e4m3
@@ -195,7 +210,9 @@ fp8_status fp8_moe_combine(const void* out, const float* w, const int32_t* pair_
 
 /* Synchronises `stream`, then returns and clears the library's device
  * status words: FP8_ERR_TIMEOUT if a kernel's bounded wait gave up since
- * the last call, FP8_ERR_CUDA if the stream reported an error, else FP8_OK. */
+ * the last call, FP8_ERR_INVALID_ARG if fp8_gemm_ue8m0 met a scale that is
+ * not a power of two, FP8_ERR_CUDA if the stream reported an error, else
+ * FP8_OK. */
 fp8_status fp8_device_status(void* stream);
 
 /* Static description of a status code. */

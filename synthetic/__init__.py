@@ -236,6 +236,12 @@ def random_e4m3_codes(shape, seed) -> np.ndarray:
     return c
 
 
+def random_pow2_scales(shape, seed, lo=-12, hi=4) -> np.ndarray:
+    """Positive power-of-two fp32 scales (the ue8m0 scale format), exponents in [lo, hi)."""
+    (r,) = _streams(seed, 1)
+    return np.exp2(r.integers(lo, hi, size=shape)).astype(np.float32)
+
+
 def random_scales(shape, seed, lo=-12, hi=4) -> np.ndarray:
     """Positive fp32 scales with a spread of exponents and full mantissas."""
     (r,) = _streams(seed, 1)
