@@ -1278,36 +1278,73 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const Tile tg = tile_of(te);
             const int row0 = tg.p_row0 + q * 32;
             const int64_t row = tg.p_row0 + e;
-#pragma unroll 1
-            for (int h = 0; h < kMxBN / 64; ++h) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h), r0);
-                tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h + 32), r1);
-                tmem_wait_ld();
-                float acc[64];
+            if (p.tma_store) {
+                // bf16 only: read the whole row out of TMEM as packed bf16
+                // (128 registers), hand the accumulator back to the MMA, then
+                // stage and store while the next tile accumulates
+                uint32_t pk[kMxBN / 2];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    acc[c] = __uint_as_float(r0[c]);
-                    acc[32 + c] = __uint_as_float(r1[c]);
+                for (int h = 0; h < kMxBN / 64; ++h) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h), r0);
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h + 32), r1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * c]), __uint_as_float(r0[2 * c + 1]));
+                        __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * c]), __uint_as_float(r1[2 * c + 1]));
+                        pk[32 * h + c] = *reinterpret_cast<uint32_t*>(&v0);
+                        pk[32 * h + 16 + c] = *reinterpret_cast<uint32_t*>(&v1);
+                    }
                 }
-                const int col0 = tg.q_row0 + 64 * h;
-                const int cols = min(64, p.N - col0);
-                if (cols <= 0) break;
-                if (p.c_bf16 && p.tma_store) {
-                    store_tile_tma<64, 32>(&tm_c, stg, lane, col0, row0, tg.p_valid - q * 32, cols, acc);
-                } else if (e < tg.p_valid) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                // 32 rows x 64 columns per box, 128-byte swizzle (16-byte chunk
+                // c of row r at c ^ (r % 8)); the TMA unit clips at M and N
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        if (c < cols) {
-                            if (p.c_bf16) p.c_bf16[row * p.N + col0 + c] = __float2bfloat16_rn(acc[c]);
-                            if (p.c_fp32) p.c_fp32[row * p.N + col0 + c] = acc[c];
+                for (int h = 0; h < kMxBN / 64; ++h) {
+                    const int col0 = tg.q_row0 + 64 * h;
+                    if (col0 >= p.N || tg.p_valid - q * 32 <= 0) break;
+                    if (lane == 0) bulk_wait_read_all();   // the previous box has left the buffer
+                    __syncwarp();
+                    uint8_t* srow = stg + lane * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(srow + ((c ^ (lane & 7)) * 16)) =
+                            make_uint4(pk[32 * h + 4 * c], pk[32 * h + 4 * c + 1], pk[32 * h + 4 * c + 2],
+                                       pk[32 * h + 4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_c, stg, col0, row0);
+                        bulk_commit();
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int h = 0; h < kMxBN / 64; ++h) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h), r0);
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h + 32), r1);
+                    tmem_wait_ld();
+                    const int col0 = tg.q_row0 + 64 * h;
+                    const int cols = min(64, p.N - col0);
+                    if (cols > 0 && e < tg.p_valid) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            if (c < cols) {
+                                const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
+                                if (p.c_bf16) p.c_bf16[row * p.N + col0 + c] = __float2bfloat16_rn(v);
+                                if (p.c_fp32) p.c_fp32[row * p.N + col0 + c] = v;
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
         }
         if (!ok) set_abort(abort_flag);
         if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_INVALID_ARG));
