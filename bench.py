@@ -281,6 +281,7 @@ def rows_measurements(fp8, torch, peaks, only=None):
         ragged_rows(fp8, torch, dev, out)
     if want("prefill_mlp"):
         prefill_row(fp8, torch, dev, fp8_peak, out)
+        prefill_row(fp8, torch, dev, fp8_peak, out, ue8m0=True)
     if want("moe"):
         moe_row(fp8, torch, dev, hbm, fp8_peak, out)
     torch.cuda.empty_cache()
@@ -336,14 +337,18 @@ def ragged_rows(fp8, torch, dev, out):
         del wk, g
 
 
-def prefill_row(fp8, torch, dev, fp8_peak, out):
-    # dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2
+def prefill_row(fp8, torch, dev, fp8_peak, out, ue8m0=False):
+    # dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2.
+    # ue8m0: every scale (weights and activations) a power of two, the GEMMs
+    # on fp8_gemm_ue8m0 (the tensor core applies the block scales)
     M, D, I = 4096, syn.MLP_DIM, syn.MLP_INTER
+    fmt = fp8.FP8_SCALE_UE8M0 if ue8m0 else fp8.FP8_SCALE_FP32
+    gemm = fp8.fp8_gemm_ue8m0 if ue8m0 else fp8.fp8_gemm
     w13q = torch.empty((2 * I, D), dtype=torch.float8_e4m3fn, device=dev)
     w13s = torch.empty((2 * I // 128, D // 128), dtype=torch.float32, device=dev)
-    fp8.fp8_weight_quant(syn.normal_bf16_device((I, D), 0.02, 1, dev), q=w13q[:I], s=w13s[: I // 128])
-    fp8.fp8_weight_quant(syn.normal_bf16_device((I, D), 0.02, 2, dev), q=w13q[I:], s=w13s[I // 128:])
-    w2q, w2s = fp8.fp8_weight_quant(syn.normal_bf16_device((D, I), 0.02, 3, dev))
+    fp8.fp8_weight_quant(syn.normal_bf16_device((I, D), 0.02, 1, dev), fmt, q=w13q[:I], s=w13s[: I // 128])
+    fp8.fp8_weight_quant(syn.normal_bf16_device((I, D), 0.02, 2, dev), fmt, q=w13q[I:], s=w13s[I // 128:])
+    w2q, w2s = fp8.fp8_weight_quant(syn.normal_bf16_device((D, I), 0.02, 3, dev), fmt)
     x = syn.normal_bf16_device((M, D), 1.0, 4, dev)
     xq = torch.empty((M, D), dtype=torch.float8_e4m3fn, device=dev)
     xs = torch.empty((M, D // 128), dtype=torch.float32, device=dev)
@@ -352,22 +357,22 @@ def prefill_row(fp8, torch, dev, fp8_peak, out):
     gsc = torch.empty((M, I // 128), dtype=torch.float32, device=dev)
     yv = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
     def mlp():
-        fp8.fp8_act_quant(x, y=xq, s=xs)
-        fp8.fp8_gemm(xq, xs, w13q, w13s, c_bf16=h13)
-        fp8.fp8_silu_mul_quant(h13, h13[:, I:], 2 * I, M, I, y=gq, s=gsc)
-        fp8.fp8_gemm(gq, gsc, w2q, w2s, c_bf16=yv)
+        fp8.fp8_act_quant(x, fmt, y=xq, s=xs)
+        gemm(xq, xs, w13q, w13s, c_bf16=h13)
+        fp8.fp8_silu_mul_quant(h13, h13[:, I:], 2 * I, M, I, fmt, y=gq, s=gsc)
+        gemm(gq, gsc, w2q, w2s, c_bf16=yv)
     g = capture(torch, mlp)
     ms = time_graph(torch, g, 10)
     flops = 3 * gemm_flops(M, I, D)
-    row = {"workload": "dense MLP M=4096, 7168->2x18432->7168", "ms": ms, "TFLOP/s": flops / ms / 1e9,
-           "frac_fp8_peak": flops / ms / 1e9 / fp8_peak}
-    g13 = capture(torch, lambda: fp8.fp8_gemm(xq, xs, w13q, w13s, c_bf16=h13))
-    g2 = capture(torch, lambda: fp8.fp8_gemm(gq, gsc, w2q, w2s, c_bf16=yv))
+    row = {"workload": "dense MLP M=4096, 7168->2x18432->7168" + (", ue8m0 scales, fp8_gemm_ue8m0" if ue8m0 else ""),
+           "ms": ms, "TFLOP/s": flops / ms / 1e9, "frac_fp8_peak": flops / ms / 1e9 / fp8_peak}
+    g13 = capture(torch, lambda: gemm(xq, xs, w13q, w13s, c_bf16=h13))
+    g2 = capture(torch, lambda: gemm(gq, gsc, w2q, w2s, c_bf16=yv))
     t13, t2 = time_graph(torch, g13, 10), time_graph(torch, g2, 10)
     f13, f2 = gemm_flops(M, 2 * I, D), gemm_flops(M, D, I)
     row["gemm_w13"] = {"ms": t13, "TFLOP/s": f13 / t13 / 1e9, "frac_fp8_peak": f13 / t13 / 1e9 / fp8_peak}
     row["gemm_w2"] = {"ms": t2, "TFLOP/s": f2 / t2 / 1e9, "frac_fp8_peak": f2 / t2 / 1e9 / fp8_peak}
-    out["prefill_mlp"] = row
+    out["prefill_mlp_ue8m0" if ue8m0 else "prefill_mlp"] = row
     del g13, g2
     del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv, g
 
@@ -472,16 +477,21 @@ def _ncu_rand_e4m3(torch, shape, gen):
     return torch.randint(0, 126, shape, dtype=torch.uint8, device="cuda", generator=gen).view(torch.float8_e4m3fn)
 
 
-def _ncu_gemm(fp8, torch, M, N, K):
+def _ncu_gemm(fp8, torch, M, N, K, ue8m0=False):
     gen = torch.Generator(device="cuda")
     gen.manual_seed(5)
     a = _ncu_rand_e4m3(torch, (M, K), gen)
     b = _ncu_rand_e4m3(torch, (N, K), gen)
-    a_s = torch.rand((M, K // 128), device="cuda", generator=gen) + 0.5
-    b_s = torch.rand(((N + 127) // 128, K // 128), device="cuda", generator=gen) + 0.5
+    if ue8m0:   # power-of-two scales for the block-scaled MMA
+        a_s = torch.exp2(torch.randint(-8, 2, (M, K // 128), device="cuda", generator=gen).float())
+        b_s = torch.exp2(torch.randint(-8, 2, ((N + 127) // 128, K // 128), device="cuda", generator=gen).float())
+    else:
+        a_s = torch.rand((M, K // 128), device="cuda", generator=gen) + 0.5
+        b_s = torch.rand(((N + 127) // 128, K // 128), device="cuda", generator=gen) + 0.5
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    gemm = fp8.fp8_gemm_ue8m0 if ue8m0 else fp8.fp8_gemm
     for _ in range(3):
-        fp8.fp8_gemm(a, a_s, b, b_s, c_bf16=c)
+        gemm(a, a_s, b, b_s, c_bf16=c)
     torch.cuda.synchronize()
     fp8.fp8_device_status()
 
@@ -517,6 +527,8 @@ NCU_CASES = {
     "decode_wq_b_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wq_b"]),
     "decode_wo_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wo"]),
     "prefill_w13": lambda fp8, torch: _ncu_gemm(fp8, torch, 4096, 2 * syn.MLP_INTER, syn.MLP_DIM),
+    "prefill_w13_ue8m0": lambda fp8, torch: _ncu_gemm(fp8, torch, 4096, 2 * syn.MLP_INTER, syn.MLP_DIM,
+                                                      ue8m0=True),
     "act_quant": _ncu_act_quant,
     "weight_dequant": _ncu_dequant,
 }
