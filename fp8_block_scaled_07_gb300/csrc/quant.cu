@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;   // independent 16-byte loads in flight per lane
+constexpr int kActUnroll = 8;   // act_quant: 8 loads in flight per lane (measured faster than 4)
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
@@ -44,15 +45,15 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
     const int sub = lane & 15;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-    for (int64_t b0 = warp * (2 * kUnroll); b0 < nblocks; b0 += nwarps * (2 * kUnroll)) {
-        uint4 v[kUnroll];
+    for (int64_t b0 = warp * (2 * kActUnroll); b0 < nblocks; b0 += nwarps * (2 * kActUnroll)) {
+        uint4 v[kActUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kActUnroll; ++u) {
             const int64_t blk = b0 + 2 * u + half;
             v[u] = blk < nblocks ? ld_stream(x + blk * 16 + sub) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kActUnroll; ++u) {
             const int64_t blk = b0 + 2 * u + half;
             float f[8];
             unpack_bf16x8(v[u], f);
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
             amax = half_warp_max(amax);
             if (blk < nblocks) {
                 const float sc = block_scale(amax, UE8M0);
-                y[blk * 16 + sub] = quant8<UE8M0>(f, sc);
+                __stcs(y + blk * 16 + sub, quant8<UE8M0>(f, sc));   // streamed out: evict first
                 if (sub == 0) s[blk] = sc;
             }
         }
@@ -113,7 +114,10 @@ __global__ void __launch_bounds__(kThreads) weight_quant_kernel(const uint16_t* 
     }
 }
 
-// Thread handles 16 consecutive codes of one row (16-byte load, 32-byte store).
+// Thread handles 16 consecutive codes of one row (16-byte load, 32-byte
+// store), kDequantUnroll of them in flight; the bf16 output is written with
+// streaming (evict-first) stores, since nothing here reads it back.
+constexpr int kDequantUnroll = 8;
 __global__ void __launch_bounds__(kThreads) weight_dequant_kernel(const uint4* __restrict__ w,
                                                                   const float* __restrict__ s,
                                                                   uint4* __restrict__ y,
@@ -125,15 +129,15 @@ __global__ void __launch_bounds__(kThreads) weight_dequant_kernel(const uint4* _
     const int64_t total = M * chunks_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    for (; c < total; c += stride * kUnroll) {
-        uint4 v[kUnroll];
+    for (; c < total; c += stride * kDequantUnroll) {
+        uint4 v[kDequantUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kDequantUnroll; ++u) {
             const int64_t cc = c + u * stride;
             v[u] = cc < total ? ld_stream(w + cc) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < kDequantUnroll; ++u) {
             const int64_t cc = c + u * stride;
             if (cc >= total) break;
             const int64_t row = cc / chunks_per_row;
@@ -151,8 +155,8 @@ __global__ void __launch_bounds__(kThreads) weight_dequant_kernel(const uint4* _
                 out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b1);
             }
             uint4* dst = y + cc * 2;
-            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            __stcs(dst, make_uint4(out[0], out[1], out[2], out[3]));
+            __stcs(dst + 1, make_uint4(out[4], out[5], out[6], out[7]));
         }
     }
 }
@@ -239,7 +243,7 @@ extern "C" fp8_status fp8_act_quant(const void* x, void* y, float* s, int64_t M,
     if (M == 0) return FP8_OK;
     if (!x || !y || !s || !aligned16(x) || !aligned16(y)) return FP8_ERR_INVALID_ARG;
     const int64_t nblocks = M * (K / kBlock);
-    const int grid = grid_for(nblocks, (kThreads / 32) * 2 * kUnroll);
+    const int grid = grid_for(nblocks, (kThreads / 32) * 2 * kActUnroll);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (scale_fmt == FP8_SCALE_UE8M0)
         launch_pdl(act_quant_kernel<true>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint4*>(x), static_cast<uint2*>(y), s, nblocks);
@@ -272,7 +276,7 @@ extern "C" fp8_status fp8_weight_dequant(const void* w, const float* s, void* y,
     if (!w || !s || !y || !aligned16(w) || !aligned16(y)) return FP8_ERR_INVALID_ARG;
     const int64_t NB = (N + kBlock - 1) / kBlock;
     const int64_t chunks = M * (N / 16);
-    const int grid = grid_for(chunks, static_cast<int64_t>(kThreads) * kUnroll);
+    const int grid = grid_for(chunks, static_cast<int64_t>(kThreads) * kDequantUnroll);
     weight_dequant_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(w), s, static_cast<uint4*>(y), M, N, NB);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
