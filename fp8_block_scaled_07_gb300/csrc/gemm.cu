@@ -423,6 +423,7 @@ __device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, cons
     const int r = qt >> 3, sub = qt & 7;
     uint32_t iter = 0;
     Seg sg;
+    griddep_wait();
     while (it.next(sg)) {
         const Tile tg = tile_geom<BN, kSwapFused>(p, sg.tile, s_prefix);
         const bool valid = r < tg.q_valid;
@@ -644,8 +645,14 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     // dependent CTA on the same SM must never take columns this one needs);
     // an otherwise idle warp signals, so the producer is not delayed
     if (threadIdx.x == 96) griddep_launch_dependents();
-    griddep_wait();   // inputs written by earlier launches are visible from here on
-    if (threadIdx.x == 0) FP8BS_TRACE(8);
+    // Inputs written by earlier launches are visible to a thread once it has
+    // passed griddepcontrol.wait.  Each role waits just before its first
+    // access to global memory, so the set-up before it overlaps the previous
+    // launch: the producer before its first load, the quantiser and the
+    // epilogue before their first scale load; the MMA issuer touches only
+    // shared and tensor memory.  The grouped kernel's tile prefix reads the
+    // offsets with the whole block, so it waits here.
+    if constexpr (V == kGrouped) griddep_wait();
     int num_tiles = p.num_tiles;
     if constexpr (V == kGrouped)
         expert_tile_prefix<C::kThreads>(p.offsets, p.G, p.N / BN, s_prefix, s_prefix + kMaxGroups + 1);
@@ -682,7 +689,11 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                         break;
                     }
                     FP8BS_TOC(w_empty, t0_);
-                    if (iter == 0) FP8BS_TRACE(2);
+                    if (iter == 0) {
+                        griddep_wait();
+                        FP8BS_TRACE(8);
+                        FP8BS_TRACE(2);
+                    }
                     if constexpr (C::kFused) {
                         // activation tile (two 64-column halves) for the quantiser
                         mbar_arrive_expect_tx(&xfull[st], C::kXTileBytes);
@@ -760,6 +771,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     } else {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
         // ---------------------------------------------------------- epilogue
+        griddep_wait();   // before its first scale load or output store
         constexpr int CPT = C::kCPT;
         const int q = warp & 3;                     // TMEM lane quarter
         const int e = q * 32 + lane;                // row of the tile (TMEM lane)
