@@ -1,0 +1,85 @@
+"""Launch ordering on one stream: every kernel of the library lets the next
+one start early (programmatic dependent launch) and waits for earlier
+launches only where it first touches global memory.  A call that reads
+buffers the previous kernel is still writing must see the new data: here
+fp8_weight_quant (which lets its dependents start at once) writes fresh
+weights and block scales, and the GEMM reading them is launched right after
+it with no host synchronisation.  Each result must equal, bit for bit, the
+same call made after a full synchronisation."""
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import fp8_block_scaled_07_gb300 as m
+    return m
+
+
+def _chained_vs_settled(fp8, call, N, K, rounds=4):
+    wq = torch.empty((N, K), dtype=torch.float8_e4m3fn, device="cuda")
+    ws = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    weights = [syn.normal_bf16_device((N, K), 0.02, 500 + i, "cuda") for i in range(rounds)]
+    torch.cuda.synchronize()
+    chained, kept = [], []
+    for i in range(rounds):
+        fp8.fp8_weight_quant(weights[i], q=wq, s=ws)   # writes the buffers the next call reads
+        chained.append(call(wq, ws).clone())
+        kept.append((wq.clone(), ws.clone()))
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+    for i, (q, s) in enumerate(kept):
+        torch.cuda.synchronize()
+        settled = call(q, s)
+        torch.cuda.synchronize()
+        assert torch.equal(chained[i].view(torch.int16), settled.view(torch.int16)), f"round {i}: stale inputs read"
+    fp8.fp8_device_status()
+
+
+@pytest.mark.parametrize("layer", ["wq_a", "wq_b", "wo"])
+def test_fused_decode_linear_reads_fresh_weights(fp8, layer):
+    N, K = syn.DECODE_LAYERS[layer]
+    x = syn.normal_bf16_device((16, K), 1.0, 510, "cuda")
+    _chained_vs_settled(fp8, lambda q, s: fp8.fp8_linear(x, q, s)[0], N, K)
+
+
+def test_staged_linear_reads_fresh_weights(fp8):
+    N, K = syn.DECODE_LAYERS["wq_a"]
+    x = syn.normal_bf16_device((48, K), 1.0, 511, "cuda")
+    _chained_vs_settled(fp8, lambda q, s: fp8.fp8_linear(x, q, s)[0], N, K)
+
+
+@pytest.mark.parametrize("M", [16, 512])
+def test_gemm_reads_fresh_weights(fp8, M):
+    # swapped decode schedule (M=16) and the dense prefill schedule (M=512)
+    N, K = 2048, 2048
+    xq, xs = fp8.fp8_act_quant(syn.normal_bf16_device((M, K), 1.0, 512 + M, "cuda"))
+    _chained_vs_settled(fp8, lambda q, s: fp8.fp8_gemm(xq, xs, q, s)[0], N, K)
+
+
+def test_gemm_reads_activations_quantised_just_before(fp8):
+    # act_quant writes the codes and scales fp8_gemm reads next, round after round
+    M, N, K = 256, 1024, 2048
+    w, w_s = fp8.fp8_weight_quant(syn.normal_bf16_device((N, K), 0.02, 520, "cuda"))
+    xq = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
+    xs = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    xs_in = [syn.normal_bf16_device((M, K), 1.0, 521 + i, "cuda") for i in range(4)]
+    torch.cuda.synchronize()
+    chained = []
+    for x in xs_in:
+        fp8.fp8_act_quant(x, y=xq, s=xs)
+        chained.append(fp8.fp8_gemm(xq, xs, w, w_s)[0].clone())
+    torch.cuda.synchronize()
+    for i, x in enumerate(xs_in):
+        q, s = fp8.fp8_act_quant(x)
+        torch.cuda.synchronize()
+        settled = fp8.fp8_gemm(q, s, w, w_s)[0]
+        torch.cuda.synchronize()
+        assert torch.equal(chained[i].view(torch.int16), settled.view(torch.int16)), f"round {i}: stale inputs read"
+    fp8.fp8_device_status()
