@@ -1075,13 +1075,15 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 //
 // 128x256 tiles, whole tiles per persistent CTA (m-fastest, as the dense
 // kernel).  Warp 0: TMA producer; warp 1: MMA issuer; warps 2-5 (one per
-// TMEM lane quarter): write each slab's scale factors into a ring of TMEM
-// slots kMxSfSlots slabs ahead of the MMA, and run each tile's epilogue.
-// TMEM: the accumulator in columns [0, 256), scale slot s at 256 + 16 s
-// (A's scales in its first 4 columns, B's in the next 8).
+// TMEM lane quarter): write each slab's scale factors into the TMEM slot of
+// its pipeline stage, and run each tile's epilogue.  A stage's barrier
+// counts the tiles' bytes and the four scale writers, so the MMA issuer
+// checks one barrier per slab (each check by the issuing thread costs tensor
+// time).  TMEM: the accumulator in columns [0, 256), the scale slot of stage
+// s at 256 + 16 s (A's scales in its first 4 columns, B's in the next 8).
 constexpr int kMxBN = 256;
 constexpr int kMxStages = 4;
-constexpr int kMxSfSlots = 8;
+constexpr int kMxSfSlots = kMxStages;   // one scale slot per stage
 constexpr int kMxThreads = 192;
 constexpr int kMxSfCol0 = 256;
 constexpr int kMxStageBytes = kPTileBytes + kMxBN * kBlock;   // A 16 KB + B 32 KB
@@ -1108,11 +1110,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint8_t* sB = smem + S * kPTileBytes;                  // S x 32 KB
     uint8_t* sStg = smem + S * kMxStageBytes;              // 4 x 4 KB output staging
     uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + kMxStgBytes);
-    uint64_t* full = bars;                      // S: operand tiles landed
+    uint64_t* full = bars;                      // S: operand tiles landed and scales written
     uint64_t* empty = bars + S;                 // S: the MMAs have read them
-    uint64_t* sf_full = bars + 2 * S;           // R: scale slot written (4 warps)
-    uint64_t* sf_empty = bars + 2 * S + R;      // R: the MMAs that read it are done
-    uint64_t* acc_full = bars + 2 * S + 2 * R;  // tile accumulated
+    uint64_t* acc_full = bars + 2 * S;          // tile accumulated
     uint64_t* acc_empty = acc_full + 1;         // accumulator read out (4 warps)
     uint64_t* mma_done = acc_full + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 4);
@@ -1122,12 +1122,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], 1 + 4);   // the producer's bytes + the four scale writers
             mbar_init(&empty[i], 1);
-        }
-        for (int i = 0; i < R; ++i) {
-            mbar_init(&sf_full[i], 4);
-            mbar_init(&sf_empty[i], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
@@ -1200,22 +1196,20 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 }
                 tc_fence_after();
                 for (uint32_t kb = 0; kb < KB; ++kb, ++iter) {
-                    const int st = static_cast<int>(iter % S), r = static_cast<int>(iter % R);
-                    if (!mbar_wait(&full[st], (iter / S) & 1, abort_flag) ||
-                        !mbar_wait(&sf_full[r], (iter / R) & 1, abort_flag)) {
+                    const int st = static_cast<int>(iter % S);
+                    if (!mbar_wait(&full[st], (iter / S) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t da = smem_desc_sw128(smem_u32(sA + st * kPTileBytes));
                     const uint64_t db = smem_desc_sw128(smem_u32(sB + st * (kMxBN * kBlock)));
-                    const uint32_t sfa = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * r);
+                    const uint32_t sfa = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * st);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)   // 4 x K=32, each with its byte of the scale words
                         mma_mx_e4m3(tmem_base, da + 2 * kk, db + 2 * kk, idesc_mx_e4m3(128, kMxBN, kk), sfa, sfa + 4,
                                     (kb > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&empty[st]);
-                    mma_commit(&sf_empty[r]);
                 }
                 if (!ok) break;
                 mma_commit(acc_full);
@@ -1266,8 +1260,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 const uint32_t wa = e8m0_code(sa, bad) * 0x01010101u;
                 const uint32_t w0 = e8m0_code(s0, bad) * 0x01010101u;
                 const uint32_t w1 = e8m0_code(s1, bad) * 0x01010101u;
+                // the stage's slot is free once the MMAs of its previous slab are done
                 const int r = static_cast<int>(iter % R);
-                if (!warp_all(mbar_wait(&sf_empty[r], ((iter / R) & 1) ^ 1, abort_flag))) {
+                if (!warp_all(mbar_wait(&empty[r], ((iter / R) & 1) ^ 1, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -1278,7 +1273,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sf_full[r]);
+                if (lane == 0) mbar_arrive(&full[r]);
             }
             if (!ok) break;
             // epilogue of tile te
