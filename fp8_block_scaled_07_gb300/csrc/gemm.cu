@@ -144,6 +144,11 @@ struct Cfg {
     static constexpr int kThreads = 128 + 32 * kEpiWarps + (kFusedV ? 64 : 0);
     static constexpr int kCPT = BN * 4 / kEpiWarps;   // accumulator columns per epilogue thread
     static constexpr bool kSplitRegs = kEpiWarps == 8;
+    // dense / grouped: the MMA issuer checks one barrier per slab (each check
+    // by the issuing thread costs tensor time): a stage's full barrier also
+    // counts the epilogue warps' release of the TMEM buffer the slab will
+    // write, i.e. of the slab two before it
+    static constexpr bool kMergeT = V == kDense || V == kGrouped;
     // the producer and MMA warps keep their tile state in registers (spills
     // there were reloaded every slab); 120*128 + 192*256 = 168*384
     static constexpr int kRegsLow = 120, kRegsHigh = 192;
@@ -597,13 +602,21 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], C::kFused ? 1 + C::kQuantWarps : 1);   // fused: TMA + the quantiser warps
+            // fused: TMA + the quantiser warps; dense / grouped: TMA + the epilogue warps
+            mbar_init(&full[i], C::kFused ? 1 + C::kQuantWarps : (C::kMergeT ? 1 + C::kEpiWarps : 1));
             mbar_init(&empty[i], 1);
             if (C::kFused) mbar_init(&xfull[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], C::kEpiWarps);   // one arrival per epilogue warp
+        }
+        if constexpr (C::kMergeT) {
+            static_assert(S >= 3, "the release of slab k-2 must land in the phase of slab k");
+            for (int w = 0; w < C::kEpiWarps; ++w) {   // slabs 0 and 1 find their TMEM buffers free
+                mbar_arrive(&full[0]);
+                mbar_arrive(&full[1]);
+            }
         }
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
@@ -731,7 +744,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     const int st = iter % S;
                     const int buf = slab & 1;
                     FP8BS_TIC(t1_);
-                    const bool te = mbar_wait(&tempty[buf], ((slab >> 1) & 1) ^ 1, abort_flag);
+                    bool te = true;
+                    if constexpr (!C::kMergeT) te = mbar_wait(&tempty[buf], ((slab >> 1) & 1) ^ 1, abort_flag);
                     FP8BS_TOC(w_tempty, t1_);
                     FP8BS_TIC(t2_);
                     const bool fu = te && mbar_wait(&full[st], (iter / S) & 1, abort_flag);
@@ -802,7 +816,12 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             FP8BS_TOC(w_promote, t4_);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
+            if (lane == 0) {
+                if constexpr (C::kMergeT)
+                    mbar_arrive(&full[(slab + 2) % S]);   // the buffer slab + 2 writes is free
+                else
+                    mbar_arrive(&tempty[buf]);
+            }
             ++slab;
             if (!warp_all(got)) {
                 set_abort(abort_flag);
