@@ -1383,6 +1383,291 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
+// The same product on CTA pairs (thread-block clusters of 2 on two SMs):
+// one 256x256 output tile per pair and tcgen05.mma.cta_group::2 of M = 256,
+// issued by the leader, twice the work per MMA (and per barrier check) of
+// the 1-SM form.  Each CTA stages its own 128 rows of A and its half of the
+// B tile (32 KB per slab), so six stages fit; each writes the scales its own
+// TMEM must hold (its 128 A rows; all 256 B columns) into its stage's slot
+// and runs the epilogue of its 128 rows.  The leader's stage barrier counts
+// both CTAs' tile bytes and all eight scale writers, so the issuer checks
+// one barrier per slab; the MMA's commits reach both CTAs.
+constexpr int kMx2Stages = 6;
+constexpr int kMx2StageBytes = 2 * kPTileBytes;   // A 128 rows + B 128 rows
+constexpr int kMx2SmemBytes = 1024 + kMx2Stages * kMx2StageBytes + kMxStgBytes + 1024;
+
+__global__ void __launch_bounds__(kMxThreads, 1)
+    gemm_mx2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_c, const Params p) {
+    constexpr int S = kMx2Stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;                                    // S x 16 KB
+    uint8_t* sB = smem + S * kPTileBytes;                  // S x 16 KB
+    uint8_t* sStg = smem + S * kMx2StageBytes;             // 4 x 4 KB output staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + kMxStgBytes);
+    uint64_t* full = bars;                      // S (leader): both CTAs' tiles landed and scales written
+    uint64_t* empty = bars + S;                 // S: the pair's MMAs have read the stage
+    uint64_t* acc_full = bars + 2 * S;          // tile accumulated
+    uint64_t* acc_empty = acc_full + 1;         // (leader) both accumulators read out (8 warps)
+    uint64_t* mma_done = acc_full + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1 + 8);   // the leader's producer (with both CTAs' bytes) + 8 scale writers
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        if (p.tma_store) tma_prefetch_desc(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();   // both CTAs' barriers exist before either arrives on the other's
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    if (threadIdx.x == 64) griddep_launch_dependents();
+    griddep_wait();
+
+    // this pair's tiles (256 x 256): cluster c takes c + i * clusters, m-fastest
+    const int cid = static_cast<int>(blockIdx.x >> 1), nclus = static_cast<int>(gridDim.x >> 1);
+    const int my_tiles = cid < p.num_tiles ? (p.num_tiles - cid + nclus - 1) / nclus : 0;
+    const uint32_t KB = static_cast<uint32_t>(p.KB);
+    const uint32_t total = static_cast<uint32_t>(my_tiles) * KB;
+    struct PT {
+        int m0, valid, n0;   // this CTA's first row and its rows inside M; the pair's first column
+    };
+    auto tile_of = [&](int ord) {
+        const int t = cid + ord * nclus;
+        const int tp = t % p.tiles_p, tq = t / p.tiles_p;
+        PT g;
+        g.m0 = tp * 256 + static_cast<int>(rank) * 128;
+        g.valid = min(128, p.M - g.m0);
+        g.n0 = tq * 256;
+        return g;
+    };
+    auto leader = [&](uint64_t* bar) { return cluster_map(smem_u32(bar), 0); };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer (each CTA)
+        if (lane == 0) {
+            uint32_t iter = 0;
+            bool ok = true;
+            for (int ord = 0; ok && ord < my_tiles; ++ord) {
+                const PT tg = tile_of(ord);
+                for (uint32_t kb = 0; kb < KB; ++kb, ++iter) {
+                    const int st = static_cast<int>(iter % S);
+                    if (!mbar_wait_cluster(&empty[st], ((iter / S) & 1) ^ 1, abort_flag)) {
+                        set_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * kMx2StageBytes);
+                    const uint32_t fb = leader(&full[st]);
+                    tma_load_2d_pair(sA + st * kPTileBytes, &tm_a, fb, static_cast<int>(kb) * kBlock, tg.m0);
+                    tma_load_2d_pair(sB + st * kPTileBytes, &tm_b, fb, static_cast<int>(kb) * kBlock,
+                                     tg.n0 + static_cast<int>(rank) * 128);
+                }
+            }
+            // the leader's barriers count both CTAs' loads: it waits for every
+            // stage it armed before the pair may end
+            if (rank == 0) {
+                const volatile int never = 0;
+                for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
+                    const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
+                    if (!mbar_wait_cluster(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer (leader)
+        if (lane == 0 && rank == 0) {
+            uint32_t iter = 0;
+            bool ok = true;
+            for (int ord = 0; ok && ord < my_tiles; ++ord) {
+                if (!mbar_wait_cluster(acc_empty, (static_cast<uint32_t>(ord) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (uint32_t kb = 0; kb < KB; ++kb, ++iter) {
+                    const int st = static_cast<int>(iter % S);
+                    if (!mbar_wait_cluster(&full[st], (iter / S) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = smem_desc_sw128(smem_u32(sA + st * kPTileBytes));
+                    const uint64_t db = smem_desc_sw128(smem_u32(sB + st * kPTileBytes));
+                    const uint32_t sfa = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * st);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_mx_e4m3_pair(tmem_base, da + 2 * kk, db + 2 * kk, idesc_mx_e4m3(256, 256, kk), sfa,
+                                         sfa + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_pair(&empty[st]);
+                }
+                if (!ok) break;
+                mma_commit_pair(acc_full);
+            }
+            if (!ok) set_abort(abort_flag);
+            mma_commit_pair(mma_done);
+            const volatile int never = 0;
+            if (!mbar_wait_cluster(mma_done, 0, &never)) set_abort(abort_flag);
+        }
+    } else {
+        // ---------------------------------------------------------- scales + epilogue (each CTA)
+        const int q = warp & 3;
+        const int e = q * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        uint8_t* stg = sStg + (warp - 2) * (32 * 128);
+        bool bad = false, ok = true;
+        float4 ca{}, cb0{}, cb1{}, na{}, nb0{}, nb1{};
+        auto load_group = [&](uint32_t slab, float4& a4, float4& b04, float4& b14) {
+            if (slab >= total) return;
+            const PT tg = tile_of(static_cast<int>(slab / KB));
+            const uint32_t kb = slab % KB;
+            const int row = tg.valid > 0 ? tg.m0 + min(e, tg.valid - 1) : 0;   // rows past M repeat a valid one
+            const int nb = tg.n0 / 128;
+            a4 = __ldg(reinterpret_cast<const float4*>(p.a_s + static_cast<int64_t>(row) * KB + kb));
+            b04 = __ldg(reinterpret_cast<const float4*>(p.b_s + static_cast<int64_t>(min(nb, p.NB - 1)) * KB + kb));
+            b14 = __ldg(reinterpret_cast<const float4*>(p.b_s + static_cast<int64_t>(min(nb + 1, p.NB - 1)) * KB + kb));
+        };
+        load_group(0, na, nb0, nb1);
+        const uint32_t full_l0 = leader(&full[0]);
+        const uint32_t acc_empty_l = leader(acc_empty);
+        uint32_t iter = 0;
+        for (int te = 0; ok && te < my_tiles; ++te) {
+            // scales up to S slabs into the next tile (their slots were last
+            // read by this tile's MMAs, which need nothing more)
+            const uint32_t limit = min(total, static_cast<uint32_t>(te + 1) * KB + min(KB, static_cast<uint32_t>(S)));
+            for (; iter < limit; ++iter) {
+                if (iter % 4 == 0) {   // KB % 4 == 0: a group never straddles two tiles
+                    ca = na;
+                    cb0 = nb0;
+                    cb1 = nb1;
+                    load_group(iter + 4, na, nb0, nb1);
+                }
+                const int j = static_cast<int>(iter % 4);
+                const float sa = j == 0 ? ca.x : j == 1 ? ca.y : j == 2 ? ca.z : ca.w;
+                const float s0 = j == 0 ? cb0.x : j == 1 ? cb0.y : j == 2 ? cb0.z : cb0.w;
+                const float s1 = j == 0 ? cb1.x : j == 1 ? cb1.y : j == 2 ? cb1.z : cb1.w;
+                const uint32_t wa = e8m0_code(sa, bad) * 0x01010101u;
+                const uint32_t w0 = e8m0_code(s0, bad) * 0x01010101u;
+                const uint32_t w1 = e8m0_code(s1, bad) * 0x01010101u;
+                // the stage's slot is free once the pair's MMAs of its previous slab are done
+                const int r = static_cast<int>(iter % S);
+                if (!warp_all(mbar_wait_cluster(&empty[r], ((iter / S) & 1) ^ 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = tmem_base + lane_off + static_cast<uint32_t>(kMxSfCol0 + 16 * r);
+                tmem_st4(col, wa, wa, wa, wa);
+                tmem_st8(col + 4, w0, w1);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote_relaxed(full_l0 + static_cast<uint32_t>(r * 8));
+            }
+            if (!ok) break;
+            if (!warp_all(mbar_wait_cluster(acc_full, static_cast<uint32_t>(te) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const PT tg = tile_of(te);
+            const int row0 = tg.m0 + q * 32;
+            const int64_t row = tg.m0 + e;
+            if (p.tma_store) {
+                uint32_t pk[128];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h), r0);
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h + 32), r1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(r0[2 * c]), __uint_as_float(r0[2 * c + 1]));
+                        __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(r1[2 * c]), __uint_as_float(r1[2 * c + 1]));
+                        pk[32 * h + c] = *reinterpret_cast<uint32_t*>(&v0);
+                        pk[32 * h + 16 + c] = *reinterpret_cast<uint32_t*>(&v1);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote_relaxed(acc_empty_l);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int col0 = tg.n0 + 64 * h;
+                    if (col0 >= p.N || tg.valid - q * 32 <= 0) break;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    uint8_t* srow = stg + lane * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(srow + ((c ^ (lane & 7)) * 16)) =
+                            make_uint4(pk[32 * h + 4 * c], pk[32 * h + 4 * c + 1], pk[32 * h + 4 * c + 2],
+                                       pk[32 * h + 4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_c, stg, col0, row0);
+                        bulk_commit();
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h), r0);
+                    tmem_ld32(tmem_base + lane_off + static_cast<uint32_t>(64 * h + 32), r1);
+                    tmem_wait_ld();
+                    const int col0 = tg.n0 + 64 * h;
+                    const int cols = min(64, p.N - col0);
+                    if (cols > 0 && e < tg.valid) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            if (c < cols) {
+                                const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
+                                if (p.c_bf16) p.c_bf16[row * p.N + col0 + c] = __float2bfloat16_rn(v);
+                                if (p.c_fp32) p.c_fp32[row * p.N + col0 + c] = v;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote_relaxed(acc_empty_l);
+            }
+        }
+        if (!ok) set_abort(abort_flag);
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_INVALID_ARG));
+        if (lane == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    cluster_sync_all();   // the peer's shared memory and TMEM stay until the pair's last MMA is done
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, 512);
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1660,29 +1945,40 @@ extern "C" fp8_status fp8_gemm_ue8m0(const void* a, const float* a_s, const void
     prm.KB = static_cast<int>(K / kBlock);
     prm.NB = static_cast<int>((N + 127) / 128);
     prm.G = 1;
-    prm.tiles_p = static_cast<int>((M + 127) / 128);
+    // CTA pairs (256 x 256 tiles) once there are enough of them to give
+    // every SM a tile; else one SM per 128 x 256 tile
+    const int sms = device_sm_count();
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + kMxBN - 1) / kMxBN);
+    const bool pairs = pair_tiles >= sms / 2 && sms >= 2;
+    prm.tiles_p = static_cast<int>(pairs ? (M + 255) / 256 : (M + 127) / 128);
     prm.tiles_q = static_cast<int>((N + kMxBN - 1) / kMxBN);
     const int64_t tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
     if (tiles > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
     prm.num_tiles = static_cast<int>(tiles);
     CUtensorMap ma, mb, mc;
-    if (!make_map(&ma, a, M, K, 128) || !make_map(&mb, b, N, K, kMxBN)) return FP8_ERR_CUDA;
+    if (!make_map(&ma, a, M, K, 128) || !make_map(&mb, b, N, K, pairs ? 128 : kMxBN)) return FP8_ERR_CUDA;
     prm.tma_store = (c_bf16 && !c_fp32 && N % 8 == 0) ? 1 : 0;
     if (prm.tma_store && !make_map_bf16(&mc, c_bf16, M, N, 32)) return FP8_ERR_CUDA;
     if (!prm.tma_store) mc = ma;   // not read
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, device_sm_count()));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    static int configured[64] = {0};
+    static int configured[64][2] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        if (cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemBytes) !=
-            cudaSuccess)
-            return FP8_ERR_CUDA;
-        configured[dev] = 1;
+    if (dev < 64 && !configured[dev][pairs ? 1 : 0]) {
+        const cudaError_t a1 =
+            pairs ? cudaFuncSetAttribute(gemm_mx2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMx2SmemBytes)
+                  : cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemBytes);
+        if (a1 != cudaSuccess) return FP8_ERR_CUDA;
+        configured[dev][pairs ? 1 : 0] = 1;
     }
-    const cudaError_t e =
-        launch_pdl_cluster(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmemBytes, st, 1u, ma, mb, mc, prm);
+    cudaError_t e;
+    if (pairs) {
+        const int grid = 2 * static_cast<int>(std::min<int64_t>(tiles, sms / 2));
+        e = launch_pdl_cluster(gemm_mx2_kernel, dim3(grid), dim3(kMxThreads), kMx2SmemBytes, st, 2u, ma, mb, mc, prm);
+    } else {
+        const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+        e = launch_pdl_cluster(gemm_mx_kernel, dim3(grid), dim3(kMxThreads), kMxSmemBytes, st, 1u, ma, mb, mc, prm);
+    }
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -134,3 +134,20 @@ def test_k_not_a_multiple_of_512_is_rejected(fp8):
     a, as_, b, bs = _case(64, 256, 384, 71)
     with pytest.raises(fp8.Fp8Error):
         fp8.fp8_gemm_ue8m0(dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs))
+
+
+@pytest.mark.parametrize("shape", [(2300, 2200, 1024), (4096, 2304, 512), (2049, 5120, 512)])
+def test_cta_pairs_ragged(fp8, shape):
+    # enough 256 x 256 tiles for the CTA-pair kernel: ragged M (the second CTA
+    # of the last pair holding some or none of the rows), ragged N, repeat
+    # calls bit-identical
+    M, N, K = shape
+    a, as_, b, bs = _case(M, N, K, 91 + M % 11)
+    args = (dev_e4m3(a), dev_f32(as_), dev_e4m3(b), dev_f32(bs))
+    cb, cf = fp8.fp8_gemm_ue8m0(*args, out_bf16=True, out_fp32=True)
+    cf2 = fp8.fp8_gemm_ue8m0(*args, out_bf16=False, out_fp32=True)[1]
+    fp8.fp8_device_status()
+    assert np.array_equal(host_f32(cf), host_f32(cf2)), f"{shape}: repeat call differs"
+    rows = np.unique(np.r_[0, 1, 127, 128, 129, 255, 256, M // 2, M - 129, M - 128, M - 2, M - 1])
+    ref, mag = oracle.gemm(a, as_, b, bs, rows=rows)
+    check_gemm(ref, mag, host_f32(cf)[rows], host_bits(cb)[rows], f"pairs {shape}")
