@@ -115,7 +115,9 @@ fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float*
  * aligned a, b, a_s and b_s (else FP8_ERR_INVALID_ARG).  Every a_s and b_s
  * value must be a positive normal power of two; any other value makes
  * fp8_device_status report FP8_ERR_INVALID_ARG, and the output is then
- * unspecified.  Meant for prefill shapes (128 x 256 output tiles). */
+ * unspecified.  Meant for prefill shapes: 256 x 256 output tiles on pairs of
+ * SMs (thread-block clusters of 2) when there is at least one such tile per
+ * SM pair, else 128 x 256 tiles on one SM each. */
 fp8_status fp8_gemm_ue8m0(const void* a, const float* a_s, const void* b, const float* b_s,
                           void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K, void* stream);
 
