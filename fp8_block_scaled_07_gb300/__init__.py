@@ -52,6 +52,9 @@ def _declare(lib):
         "fp8_moe_combine": (st, [vp, f32p, vp, i64, i32, i64, vp, f32p, vp]),
         "fp8_linear_workspace_size": (sz, [i64, i64, i64]),
         "fp8_linear": (st, [vp, vp, f32p, vp, f32p, i64, i64, i64, ctypes.c_int, vp, sz, vp]),
+        "fp8_gemm_noalloc": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, vp]),
+        "fp8_debug_set_wait_limit": (st, [ctypes.c_longlong]),
+        "fp8_debug_skip_one_arrive": (None, []),
         "fp8_device_status": (st, [vp]),
         "fp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "fp8_num_sms": (ctypes.c_int, []),

@@ -23,6 +23,11 @@ constexpr float kAmaxFloor = 1e-4f;    // clamp on a block's max |x|
 
 // ~1 s at 2 GHz: far above any legitimate wait inside one kernel.
 constexpr long long kWaitLimitCycles = 2000000000LL;
+// The limit the waits use (SM clock cycles).  Only the test hook
+// fp8_debug_set_wait_limit changes it, so that a test of the failure path
+// ends in milliseconds; one copy per translation unit (the GEMM's is the one
+// that matters: its kernels are the ones that wait).
+static __device__ long long g_wait_limit_cycles = kWaitLimitCycles;
 
 #define FP8_CUDA_TRY(expr)                                   \
     do {                                                     \
@@ -205,7 +210,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0u) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) return false;
+            if (clock64() - t0 > g_wait_limit_cycles) return false;
         }
     }
 }
@@ -487,7 +492,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
         if (ok) return true;
         if ((it & 63u) == 0u) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) return false;
+            if (clock64() - t0 > g_wait_limit_cycles) return false;
         }
     }
 }

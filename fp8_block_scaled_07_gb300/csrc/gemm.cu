@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -111,6 +112,7 @@ struct Params {
     int ue8m0;                 // fused: activation scale format
     int tma_store;             // dense, bf16 only: full tiles leave through shared memory and TMA
     int vec_scales;            // scale rows are 16-byte aligned (K/128 % 4 == 0, aligned bases)
+    int debug_skip;            // test hook: the MMA issuer skips its arrive on slab 0's TMEM-full barrier
 };
 
 struct Tile {
@@ -764,7 +766,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     for (int kk = 0; kk < 4; ++kk)   // 4 x K=32 = one 128-K slab; +32 bytes each
                         mma_e4m3(d, da + 2 * kk, db + 2 * kk, idesc, kk > 0 ? 1u : 0u);
                     mma_commit(&empty[st]);
-                    mma_commit(&tfull[buf]);
+                    // (a test of the failure path withholds slab 0's
+                    // hand-off: the epilogue's wait must run out)
+                    if (!(p.debug_skip && slab == 0)) mma_commit(&tfull[buf]);
                 }
             }
             FP8BS_TRACE_VAL(12, static_cast<unsigned long long>(w_tempty));
@@ -1852,14 +1856,27 @@ extern "C" int fp8_debug_read_trace(unsigned long long* host) {
 }
 #endif
 
+// Test hooks of the failure path (see fp8_debug_skip_one_arrive).
+static std::atomic<int> g_debug_skip_next{0};
+
+extern "C" fp8_status fp8_debug_set_wait_limit(long long cycles) {
+    const long long v = cycles > 0 ? cycles : kWaitLimitCycles;
+    return cudaMemcpyToSymbol(g_wait_limit_cycles, &v, sizeof(v)) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" void fp8_debug_skip_one_arrive(void) { g_debug_skip_next.store(1); }
+
 extern "C" size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kBlock != 0) return 0;
     return make_plan(M, N, K, device_sm_count()).ws_bytes;
 }
 
-extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
-                               void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// fp8_gemm's argument checks, shared with fp8_gemm_noalloc so that a call
+// either of them rejects touches nothing on the device.  FP8_OK with M == 0
+// or N == 0 means there is nothing to do.
+fp8_status gemm_check_args(const void* a, const float* a_s, const void* b, const float* b_s, const void* c_bf16,
+                           const float* c_fp32, int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return FP8_OK;
     if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
@@ -1870,6 +1887,15 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
         return FP8_ERR_INVALID_ARG;
     if (N % 8 == 0 && ((c_bf16 && !aligned16(c_bf16)) || (c_fp32 && !aligned16(c_fp32))))
         return FP8_ERR_INVALID_ARG;
+    return FP8_OK;
+}
+}  // namespace
+
+extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
+                               void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    const fp8_status chk = gemm_check_args(a, a_s, b, b_s, c_bf16, c_fp32, M, N, K);
+    if (chk != FP8_OK || M == 0 || N == 0) return chk;
     const Plan pl = make_plan(M, N, K, device_sm_count());
     if (pl.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pl.ws_bytes))
         return FP8_ERR_WORKSPACE;
@@ -1891,6 +1917,7 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     prm.total_units = pl.total_units;
     prm.ksplit = pl.ksplit;
     prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(b_s)) ? 1 : 0;
+    prm.debug_skip = g_debug_skip_next.exchange(0);
 #ifdef FP8BS_TRACE_ENABLED
     prm.trace_slot = g_trace_next++ & 3;
 #endif
@@ -2061,8 +2088,10 @@ fp8_status noalloc_scratch(void** out) {
 extern "C" fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const void* b,
                                        const float* b_s, void* c_bf16, float* c_fp32, int64_t M,
                                        int64_t N, int64_t K, void* stream) {
-    if (M < 0 || N < 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return FP8_OK;
+    // every check fp8_gemm makes comes first: a rejected call leaves the
+    // shared array alone (it may belong to a call running on another stream)
+    const fp8_status chk = gemm_check_args(a, a_s, b, b_s, c_bf16, c_fp32, M, N, K);
+    if (chk != FP8_OK || M == 0 || N == 0) return chk;
     const size_t need = fp8_gemm_workspace_size(M, N, K);
     if (need > kNoAllocScratchBytes) return FP8_ERR_WORKSPACE;   // beyond the fixed array
     void* scratch = nullptr;

@@ -154,10 +154,12 @@ fp8_status fp8_linear(const void* x, const void* w, const float* w_s, void* c_bf
  *   - Shapes whose split-K schedule needs more scratch than the array holds
  *     (fp8_gemm_workspace_size(M, N, K) > 8 MiB) return FP8_ERR_WORKSPACE and
  *     launch nothing; use fp8_gemm with a caller workspace for those.
- *   - Every call clears the counters it needs on `stream` and then uses the
- *     shared array: calls that may overlap on the GPU (different streams,
- *     different host threads) race on it and must be serialised by the
- *     caller.  No cudaMalloc, cudaFree or allocating routine is called. */
+ *   - Arguments are checked first, exactly as fp8_gemm checks them; a call
+ *     that returns an error has enqueued nothing and left the array alone.
+ *   - Every accepted call clears the counters it needs on `stream` and then
+ *     uses the shared array: calls that may overlap on the GPU (different
+ *     streams, different host threads) race on it and must be serialised by
+ *     the caller.  No cudaMalloc, cudaFree or allocating routine is called. */
 fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const void* b, const float* b_s,
                             void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K,
                             void* stream);
@@ -216,6 +218,21 @@ fp8_status fp8_moe_combine(const void* out, const float* w, const int32_t* pair_
  * not a power of two, FP8_ERR_CUDA if the stream reported an error, else
  * FP8_OK. */
 fp8_status fp8_device_status(void* stream);
+
+/* Test hooks of the failure path (no counterpart in the pages: they exist so
+ * that a test can make a kernel's bounded wait run out without faulting or
+ * hanging the GPU).  fp8_debug_set_wait_limit sets, on the current device,
+ * how many SM clock cycles a kernel waits on one barrier before it gives up
+ * (cycles <= 0 restores the default of 2e9, about a second); it copies to
+ * device memory synchronously, so call it with no library kernel running.
+ * fp8_debug_skip_one_arrive makes the next fp8_gemm call (and only that one)
+ * withhold the tensor core's hand-off of its first 128-K slab to the
+ * epilogue: the epilogue's wait runs out, the kernel winds down (waits for
+ * its own copies and MMAs, frees its tensor memory, returns) and
+ * fp8_device_status then reports FP8_ERR_TIMEOUT; that call's output is
+ * unspecified.  Neither is meant for production use. */
+fp8_status fp8_debug_set_wait_limit(long long cycles);
+void fp8_debug_skip_one_arrive(void);
 
 /* Static description of a status code. */
 const char* fp8_status_string(fp8_status status);

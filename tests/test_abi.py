@@ -59,6 +59,11 @@ def test_host_validation_rejects_bad_arguments(fp8):
     assert L.fp8_silu_mul_quant(NULL, NULL, 256, 4, 100, NULL, NULL, NULL, 0, NULL) == 1
     assert L.fp8_moe_route(NULL, 4, 8, 2000, NULL, NULL, NULL, NULL) == 1
     assert L.fp8_moe_combine(NULL, NULL, NULL, 4, 8, 12, NULL, NULL, NULL) == 1
+    # fp8_gemm_noalloc checks its arguments before it touches the device
+    assert L.fp8_gemm_noalloc(NULL, NULL, NULL, NULL, NULL, NULL, 4, 4, 100, NULL) == 1
+    assert L.fp8_gemm_noalloc(NULL, NULL, NULL, NULL, NULL, NULL, 4, 4, 128, NULL) == 1
+    assert L.fp8_gemm_noalloc(ctypes.c_void_p(8), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                              ctypes.c_void_p(16), NULL, 4, 4, 128, NULL) == 1
     # fp8_linear: unknown scale format
     assert L.fp8_linear(NULL, NULL, NULL, NULL, NULL, 4, 4, 128, 7, NULL, 0, NULL) == 1
 

@@ -1,9 +1,11 @@
 """fp8_gemm_noalloc: the GEMM for callers that cannot give the library a
 workspace (no cudaMalloc allowed on their path, a fixed memory budget, or an
 allocator that hands out no scratch).  Its split-tile scratch is a fixed
-8 MiB array inside the library, so the result must match fp8_gemm with a
-caller workspace, and two calls in a row (the second finding the first
-one's leftovers in the shared array) must both be right.
+8 MiB array inside the library.  It runs the same plan and the same
+fixed-order reduction as fp8_gemm, so its outputs must equal fp8_gemm's with
+a caller workspace bit for bit; two calls in a row on the same split shape
+with different data (the second reusing the partial tiles the first left in
+the shared array) must both be exact.
 
 Called through the C ABI with ctypes.  Kept in its own file, collected last."""
 import ctypes
@@ -52,13 +54,14 @@ def _case(M, N, K, seed):
 
 
 def test_two_calls_in_a_row_match_the_workspace_entry_point(fp8):
-    # two shapes with few output tiles: K is split across CTAs with partial
-    # tiles in the scratch (the second call finds the first one's leftovers)
-    cases = [(300, 384, 1024), (129, 136, 256)]
+    # shapes with few output tiles: K is split across CTAs with partial tiles
+    # in the scratch.  Each shape runs twice in a row with different data, so
+    # the second call overwrites the partials the first one left behind.
+    cases = [(300, 384, 1024, 40), (300, 384, 1024, 60), (129, 136, 256, 50), (129, 136, 256, 70)]
     results = []
-    for i, (M, N, K) in enumerate(cases):
-        name = f"{M}x{N}x{K}"
-        aq, as_, bq, bs = _case(M, N, K, 40 + 10 * i)
+    for M, N, K, seed in cases:
+        name = f"{M}x{N}x{K} seed {seed}"
+        aq, as_, bq, bs = _case(M, N, K, seed)
         assert 0 < fp8.fp8_gemm_workspace_size(M, N, K) <= SCRATCH_BYTES
         args = (dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs))
         st, cb, cf = _noalloc(fp8, *args, M, N, K)
@@ -70,8 +73,27 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(fp8):
         check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"noalloc {name}")
         wb, wf = fp8.fp8_gemm(*args, out_bf16=True, out_fp32=True)
         fp8.fp8_device_status()
-        diff = np.abs(host_f32(cf).astype(np.float64) - host_f32(wf))
-        assert np.all(diff <= 1e-4 * mag), f"{name}: noalloc differs from fp8_gemm"
+        assert np.array_equal(host_f32(cf).view(np.uint32), host_f32(wf).view(np.uint32)), \
+            f"{name}: fp32 output differs from fp8_gemm's"
+        assert np.array_equal(host_bits(cb), host_bits(wb)), f"{name}: bf16 output differs from fp8_gemm's"
+
+
+def test_rejected_call_enqueues_nothing(fp8):
+    # a misaligned operand is rejected before the shared array is touched
+    M, N, K = 300, 384, 1024
+    aq, as_, bq, bs = _case(M, N, K, 80)
+    a, s_a, b, s_b = dev_e4m3(aq), dev_f32(as_), dev_e4m3(bq), dev_f32(bs)
+    raw = torch.empty(M * K + 16, dtype=torch.uint8, device="cuda")
+    a_mis = raw[1:1 + M * K].view(M, K)
+    st, _, _ = _noalloc(fp8, a_mis, s_a, b, s_b, M, N, K)
+    assert st == 1   # FP8_ERR_INVALID_ARG
+    # the next call still finds clean counters and is exact
+    st, cb, cf = _noalloc(fp8, a, s_a, b, s_b, M, N, K)
+    assert st == 0
+    fp8.fp8_device_status()
+    wb, wf = fp8.fp8_gemm(a, s_a, b, s_b, out_bf16=True, out_fp32=True)
+    fp8.fp8_device_status()
+    assert np.array_equal(host_f32(cf).view(np.uint32), host_f32(wf).view(np.uint32))
 
 
 def test_shapes_needing_more_scratch_are_rejected(fp8):
