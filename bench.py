@@ -6,8 +6,9 @@ with bf16 activations ~N(0,1) (0.5% outliers x30) and e4m3 weights with
 128x128 fp32 block scales drawn from N(0, 0.02).  One step = act_quant +
 fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer,
 each one kernel at this batch (the quantisation runs inside the GEMM) --
-three launches, replayed from CUDA graphs.  Four weight sets (4 x 167 MB) rotate between steps so
-every step streams its weights from HBM (inputs larger than L2).
+three launches per step, replayed from CUDA graphs of four consecutive
+steps.  Four weight sets (4 x 167 MB) rotate between steps so every step
+streams its weights from HBM (inputs larger than L2).
 
 value  = algorithmic HBM bytes of the step / device time (GB/s); the
          algorithmic bytes are what the method must move at least: e4m3
@@ -21,7 +22,12 @@ roofline = the dominant kernel, wo's fused linear kernel (the largest share
          graph of its four weight-rotation launches, replayed right after
          the timed region; the other layers' kernels are timed the same way
          and listed beside it;
-cpu_baseline = the CPU oracle on the host cores over a bounded sample.
+cpu_baseline = the CPU oracle on the host cores over a bounded sample (all
+         cores, and one core), plus its GEMM rate on 128-row subsets of the
+         prefill and MoE workloads;
+rows   = every other hot-path row on its own workload (decode at M = 1,
+         16 and 64, act_quant, weight_dequant, ragged ue8m0, the prefill
+         MLP, MoE), each the median of five timed windows with the spread.
 
 With --impl reference the CPU oracle itself is timed on the same workload
 (each step a bounded sample: all three layers' act_quant and 1/16 of each
@@ -90,9 +96,16 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of every source the library is built from (all kernels, the
+    shared header, the C ABI header): a committed ncu traffic figure counts
+    only while it matches."""
     h = hashlib.sha256()
-    for name in ("gemm.cu", "common.cuh"):
-        with open(os.path.join(ROOT, "fp8_block_scaled_07_gb300", "csrc", name), "rb") as f:
+    csrc = os.path.join(ROOT, "fp8_block_scaled_07_gb300", "csrc")
+    paths = sorted(os.path.join(csrc, n) for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
+    paths.append(os.path.join(ROOT, "include", "fp8bs.h"))
+    for path in paths:
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -245,6 +258,35 @@ def oracle_decode_sample(torch, dec, fraction_den, rotation=0):
     return time.perf_counter() - t0, nbytes, flops
 
 
+def _omp_set_threads(n):
+    """Set the oracle's OpenMP thread count (libgomp is loaded with it)."""
+    import ctypes
+    try:
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+        return True
+    except (OSError, AttributeError):
+        return False
+
+
+def oracle_gemm_subsets():
+    """The oracle's GEMM on fixed 128-row subsets of the prefill and MoE
+    workloads, in GFLOP/s: prefill = 128 tokens against the first 2048
+    output features of w1 (K = 7168); MoE = 128 rows of one expert's w2
+    (K = 2048 -> N = 7168).  Inputs drawn and quantised on the host."""
+    import oracle
+    rs = np.random.default_rng(syn.SEED_BASE + 9)
+    res = {}
+    for key, (Mr, N, K) in (("prefill_w1_128rows", (128, 2048, syn.MLP_DIM)),
+                            ("moe_w2_128rows", (128, syn.MOE_DIM, syn.MOE_INTER))):
+        aq, as_ = oracle.act_quant(syn.normal_bf16(rs, (Mr, K), 1.0))
+        wq, ws = oracle.weight_quant(syn.normal_bf16(rs, (N, K), 0.02))
+        t0 = time.perf_counter()
+        oracle.gemm(aq, as_, wq, ws)
+        dt = time.perf_counter() - t0
+        res[key + "_GFLOP/s"] = gemm_flops(Mr, N, K) / dt / 1e9
+    return res
+
+
 def omp_threads():
     v = os.environ.get("OMP_NUM_THREADS")
     return int(v) if v and v.isdigit() else (os.cpu_count() or 1)
@@ -263,15 +305,28 @@ def time_graph(torch, g, iters):
     return s.elapsed_time(e) / iters
 
 
-def rows_measurements(fp8, torch, peaks, only=None):
-    """Every other hot-path row on its own workload (device time)."""
+WINDOWS = 5
+
+
+def time_windows(torch, g, iters, windows=WINDOWS):
+    """ms per replay: the median of `windows` timed windows of `iters`
+    replays each, with the spread (min, max) over the windows."""
+    v = sorted(time_graph(torch, g, iters) for _ in range(windows))
+    return {"median": v[len(v) // 2], "min": v[0], "max": v[-1], "windows": windows, "replays": iters}
+
+
+def rows_measurements(fp8, torch, peaks, only=None, dec=None):
+    """Every other hot-path row on its own workload (device time); each
+    figure is the median of WINDOWS timed windows, with their spread."""
     def want(name):
         return only is None or name in only
     dev = torch.device("cuda")
     hbm = peaks["hbm_gbs"]
-    fp8_peak = 2.0 * peaks["bf16_tflops"]           # dense fp8 = 2x dense bf16 (nominal ratio)
+    fp8_peak = 2.0 * peaks["bf16_tflops"]                      # dense fp8 = 2x dense bf16 (nominal ratio)
+    fp8_peak_sus = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     out = {}
-
+    if want("decode") and dec is not None:
+        decode_rows(fp8, torch, dec, hbm, out)
     # act_quant alone, prefill-sized input larger than L2 (4096 x 18432 bf16 = 151 MB)
     if want("act_quant"):
         act_quant_row(fp8, torch, dev, hbm, out)
@@ -280,24 +335,80 @@ def rows_measurements(fp8, torch, peaks, only=None):
     if want("ragged"):
         ragged_rows(fp8, torch, dev, out)
     if want("prefill_mlp"):
-        prefill_row(fp8, torch, dev, fp8_peak, out)
-        prefill_row(fp8, torch, dev, fp8_peak, out, ue8m0=True)
+        prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out)
+        prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=True)
     if want("moe"):
         moe_row(fp8, torch, dev, hbm, fp8_peak, out)
     torch.cuda.empty_cache()
     return out
 
 
+def _rate(t, amount, scale):
+    """{median, min, max} of a rate from {median, min, max} times (ms)."""
+    return {"median": amount / t["median"] / scale, "min": amount / t["max"] / scale,
+            "max": amount / t["min"] / scale}
+
+
+def decode_rows(fp8, torch, dec, hbm, out):
+    """Config 2 at every batch it names (M = 1, 16, 64): per layer the
+    fp8_linear call (one kernel where the quantisation is fused, else
+    act_quant + GEMM) and the whole three-layer step, over the same four
+    rotating weight sets as the headline."""
+    dev = torch.device("cuda")
+    for M in (1, 16, 64):
+        xs = [{n: syn.normal_bf16_device((M, syn.DECODE_LAYERS[n][1]), 1.0, 7000 + 100 * M + 10 * r + i, dev,
+                                         outlier_frac=0.005, outlier_mult=30.0)
+               for i, n in enumerate(LAYERS)} for r in range(dec.R)]
+        ys = {n: torch.empty((M, syn.DECODE_LAYERS[n][0]), dtype=torch.bfloat16, device=dev) for n in LAYERS}
+        need = max(int(fp8.lib.fp8_linear_workspace_size(M, *syn.DECODE_LAYERS[n])) for n in LAYERS)
+        ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+        row = {"workload": f"decode linears M={M}, 4 rotating weight sets (668 MB)", "layers": {}}
+        for name in LAYERS:
+            N, K = syn.DECODE_LAYERS[name]
+
+            def calls(name=name):
+                for r in range(dec.R):
+                    wq, wsc = dec.w[r][name]
+                    fp8.fp8_linear(xs[r][name], wq, wsc, c_bf16=ys[name], workspace=ws)
+            g = capture(torch, calls)
+            t = time_windows(torch, g, 50)
+            t = {k: (v / dec.R if k in ("median", "min", "max") else v) for k, v in t.items()}
+            b = linear_bytes(M, N, K)
+            fused = int(fp8.lib.fp8_linear_workspace_size(M, N, K)) == 0
+            row["layers"][name] = {"us": t["median"] * 1e3, "us_min": t["min"] * 1e3, "us_max": t["max"] * 1e3,
+                                   "GB/s": b / t["median"] / 1e6, "frac_hbm": b / t["median"] / 1e6 / hbm,
+                                   "kernels": 1 if fused else 2}
+            del g
+
+        def steps():
+            for r in range(dec.R):
+                for name in LAYERS:
+                    wq, wsc = dec.w[r][name]
+                    fp8.fp8_linear(xs[r][name], wq, wsc, c_bf16=ys[name], workspace=ws)
+        g = capture(torch, steps)
+        t = time_windows(torch, g, 50)
+        step_ms = t["median"] / dec.R
+        b = decode_step_bytes(M)
+        row["step_us"] = step_ms * 1e3
+        row["step_us_min"], row["step_us_max"] = t["min"] / dec.R * 1e3, t["max"] / dec.R * 1e3
+        row["step_GB/s"] = b / step_ms / 1e6
+        row["step_frac_hbm"] = b / step_ms / 1e6 / hbm
+        out[f"decode_M{M}"] = row
+        del g, xs, ys, ws
+
+
 def act_quant_row(fp8, torch, dev, hbm, out):
     xa = [syn.normal_bf16_device((4096, 18432), 1.0, 77 + i, dev) for i in range(2)]
     ya = torch.empty((4096, 18432), dtype=torch.float8_e4m3fn, device=dev)
     sa = torch.empty((4096, 144), dtype=torch.float32, device=dev)
-    gs = [capture(torch, lambda i=i: fp8.fp8_act_quant(xa[i], y=ya, s=sa)) for i in range(2)]
-    ms = sum(time_graph(torch, g, 20) for g in gs) / 2
+    g = capture(torch, lambda: [fp8.fp8_act_quant(xa[i], y=ya, s=sa) for i in range(2)])
+    t = time_windows(torch, g, 20)
+    t = {k: (v / 2 if k in ("median", "min", "max") else v) for k, v in t.items()}
     b = act_quant_bytes(4096, 18432)
-    out["act_quant"] = {"workload": "4096x18432 bf16", "us": ms * 1e3, "GB/s": b / ms / 1e6,
-                        "frac_hbm": b / ms / 1e6 / hbm}
-    del xa, ya, sa, gs
+    out["act_quant"] = {"workload": "4096x18432 bf16 (two inputs alternating, 302 MB > L2)",
+                        "us": t["median"] * 1e3, "us_min": t["min"] * 1e3, "us_max": t["max"] * 1e3,
+                        "GB/s": b / t["median"] / 1e6, "frac_hbm": b / t["median"] / 1e6 / hbm}
+    del xa, ya, sa, g
 
 
 def dequant_row(fp8, torch, dev, hbm, out):
@@ -306,10 +417,11 @@ def dequant_row(fp8, torch, dev, hbm, out):
     del w
     yd = torch.empty((18432, 7168), dtype=torch.bfloat16, device=dev)
     g = capture(torch, lambda: fp8.fp8_weight_dequant(wq, ws, y=yd))
-    ms = time_graph(torch, g, 20)
+    t = time_windows(torch, g, 20)
     b = 18432 * 7168 * 3 + 4 * 144 * 56
-    out["weight_dequant"] = {"workload": "18432x7168 e4m3 -> bf16", "us": ms * 1e3, "GB/s": b / ms / 1e6,
-                             "frac_hbm": b / ms / 1e6 / hbm}
+    out["weight_dequant"] = {"workload": "18432x7168 e4m3 -> bf16 (396 MB > L2)", "us": t["median"] * 1e3,
+                             "us_min": t["min"] * 1e3, "us_max": t["max"] * 1e3,
+                             "GB/s": b / t["median"] / 1e6, "frac_hbm": b / t["median"] / 1e6 / hbm}
     del wq, ws, yd, g
 
 
@@ -329,18 +441,22 @@ def ragged_rows(fp8, torch, dev, out):
                 fp8.fp8_act_quant(x, fp8.FP8_SCALE_UE8M0, y=xq, s=xs)
                 fp8.fp8_gemm(xq, xs, wk[i][0], wk[i][1], c_bf16=y, workspace=wsb)
         g = capture(torch, run)
-        ms = time_graph(torch, g, 5) / copies
+        t = time_windows(torch, g, 5)
+        ms = t["median"] / copies
         b = act_quant_bytes(M, 7168) + gemm_bytes(M, 576, 7168)
         f = gemm_flops(M, 576, 7168)
-        out[f"ragged_ue8m0_M{M}"] = {"workload": f"wkv_a 7168->576 M={M} ue8m0", "us": ms * 1e3,
+        out[f"ragged_ue8m0_M{M}"] = {"workload": f"wkv_a 7168->576 M={M} ue8m0 (act_quant + fp8_gemm)",
+                                     "us": ms * 1e3, "us_min": t["min"] / copies * 1e3,
+                                     "us_max": t["max"] / copies * 1e3,
                                      "GB/s": b / ms / 1e6, "TFLOP/s": f / ms / 1e9}
         del wk, g
 
 
-def prefill_row(fp8, torch, dev, fp8_peak, out, ue8m0=False):
+def prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=False):
     # dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2.
     # ue8m0: every scale (weights and activations) a power of two, the GEMMs
-    # on fp8_gemm_ue8m0 (the tensor core applies the block scales)
+    # on fp8_gemm_ue8m0 (the tensor core applies the block scales): the
+    # scale_fmt "ue8m0" reading extended to the weights, not config 3 itself
     M, D, I = 4096, syn.MLP_DIM, syn.MLP_INTER
     fmt = fp8.FP8_SCALE_UE8M0 if ue8m0 else fp8.FP8_SCALE_FP32
     gemm = fp8.fp8_gemm_ue8m0 if ue8m0 else fp8.fp8_gemm
@@ -356,22 +472,32 @@ def prefill_row(fp8, torch, dev, fp8_peak, out, ue8m0=False):
     gq = torch.empty((M, I), dtype=torch.float8_e4m3fn, device=dev)
     gsc = torch.empty((M, I // 128), dtype=torch.float32, device=dev)
     yv = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+
     def mlp():
         fp8.fp8_act_quant(x, fmt, y=xq, s=xs)
         gemm(xq, xs, w13q, w13s, c_bf16=h13)
         fp8.fp8_silu_mul_quant(h13, h13[:, I:], 2 * I, M, I, fmt, y=gq, s=gsc)
         gemm(gq, gsc, w2q, w2s, c_bf16=yv)
     g = capture(torch, mlp)
-    ms = time_graph(torch, g, 10)
+    t = time_windows(torch, g, 10)
     flops = 3 * gemm_flops(M, I, D)
-    row = {"workload": "dense MLP M=4096, 7168->2x18432->7168" + (", ue8m0 scales, fp8_gemm_ue8m0" if ue8m0 else ""),
-           "ms": ms, "TFLOP/s": flops / ms / 1e9, "frac_fp8_peak": flops / ms / 1e9 / fp8_peak}
+    what = ("dense MLP M=4096, 7168->2x18432->7168, " +
+            ("ue8m0 scales on weights and activations, fp8_gemm_ue8m0 (outside config 3, whose weights carry "
+             "fp32 scales)" if ue8m0 else "fp32 scales (config 3), fp8_gemm"))
+    tf = _rate(t, flops, 1e9)
+    # the chain is a 1.1-1.4 ms replay loop: quoted against both the burst and
+    # the sustained (power-capped) dense fp8 peak
+    row = {"workload": what, "ms": t["median"], "ms_min": t["min"], "ms_max": t["max"],
+           "TFLOP/s": tf["median"], "TFLOP/s_min": tf["min"], "TFLOP/s_max": tf["max"],
+           "frac_fp8_peak": tf["median"] / fp8_peak, "frac_fp8_peak_sustained": tf["median"] / fp8_peak_sus}
     g13 = capture(torch, lambda: gemm(xq, xs, w13q, w13s, c_bf16=h13))
     g2 = capture(torch, lambda: gemm(gq, gsc, w2q, w2s, c_bf16=yv))
-    t13, t2 = time_graph(torch, g13, 10), time_graph(torch, g2, 10)
-    f13, f2 = gemm_flops(M, 2 * I, D), gemm_flops(M, D, I)
-    row["gemm_w13"] = {"ms": t13, "TFLOP/s": f13 / t13 / 1e9, "frac_fp8_peak": f13 / t13 / 1e9 / fp8_peak}
-    row["gemm_w2"] = {"ms": t2, "TFLOP/s": f2 / t2 / 1e9, "frac_fp8_peak": f2 / t2 / 1e9 / fp8_peak}
+    for key, gg, f in (("gemm_w13", g13, gemm_flops(M, 2 * I, D)), ("gemm_w2", g2, gemm_flops(M, D, I))):
+        tt = time_windows(torch, gg, 10)
+        r = _rate(tt, f, 1e9)
+        row[key] = {"ms": tt["median"], "ms_min": tt["min"], "ms_max": tt["max"], "TFLOP/s": r["median"],
+                    "TFLOP/s_min": r["min"], "TFLOP/s_max": r["max"], "frac_fp8_peak": r["median"] / fp8_peak,
+                    "frac_fp8_peak_sustained": r["median"] / fp8_peak_sus}
     out["prefill_mlp_ue8m0" if ue8m0 else "prefill_mlp"] = row
     del g13, g2
     del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv, g
@@ -408,18 +534,35 @@ def moe_row(fp8, torch, dev, hbm, fp8_peak, out):
         st.update(off=off, aq=aq, as_=as_, h=h, gq=gq_, gs=gs_, o2=o2)
         st["y"] = fp8.fp8_moe_combine(o2, wts, pr)[0]
     g = capture(torch, moe)
-    ms = time_graph(torch, g, 5)
+    t = time_windows(torch, g, 5)
+    ms = t["median"]
     flops = R * (gemm_flops(1, 2 * I, D) + gemm_flops(1, D, I))
     wbytes = E * (2 * I * D + D * I)
-    row = {"workload": "MoE 4096 tok x top-8 of 256, 7168->2x2048->7168", "ms": ms,
+    row = {"workload": "MoE 4096 tok x top-8 of 256 (Zipf routing), 7168->2x2048->7168", "ms": ms,
+           "ms_min": t["min"], "ms_max": t["max"],
            "TFLOP/s": flops / ms / 1e9, "weight_GB/s": wbytes / ms / 1e6,
            "roofline_ms": max(wbytes / hbm / 1e6, flops / fp8_peak / 1e9)}
-    g13 = capture(torch, lambda: fp8.fp8_grouped_gemm(st["aq"], st["as_"], w13q, w13s, st["off"], c_bf16=st["h"]))
-    g2 = capture(torch, lambda: fp8.fp8_grouped_gemm(st["gq"], st["gs"], w2q, w2s, st["off"], c_bf16=st["o2"]))
-    row["grouped_w13_ms"] = time_graph(torch, g13, 5)
-    row["grouped_w2_ms"] = time_graph(torch, g2, 5)
+    row["frac_roofline"] = row["roofline_ms"] / ms
+    # each stage on its own (same inputs as inside the chain)
+    stages = {
+        "route": lambda: fp8.fp8_moe_route(ids, E),
+        "act_quant": lambda: fp8.fp8_act_quant(x, y=xq, s=xs),
+        "gather": lambda: fp8.fp8_moe_gather(xq, xs, st_rt[2], aq=st["aq"], as_=st["as_"]),
+        "grouped_w13": lambda: fp8.fp8_grouped_gemm(st["aq"], st["as_"], w13q, w13s, st["off"], c_bf16=st["h"]),
+        "silu_mul_quant": lambda: fp8.fp8_silu_mul_quant(st["h"], st["h"][:, I:], 2 * I, R, I, y=st["gq"],
+                                                         s=st["gs"]),
+        "grouped_w2": lambda: fp8.fp8_grouped_gemm(st["gq"], st["gs"], w2q, w2s, st["off"], c_bf16=st["o2"]),
+        "combine": lambda: fp8.fp8_moe_combine(st["o2"], wts, st_rt[1]),
+    }
+    st_rt = fp8.fp8_moe_route(ids, E)
+    row["stages_ms"] = {}
+    for name, fn in stages.items():
+        gs = capture(torch, fn)
+        row["stages_ms"][name] = time_windows(torch, gs, 5)["median"]
+        del gs
+    row["grouped_w13_ms"] = row["stages_ms"]["grouped_w13"]
+    row["grouped_w2_ms"] = row["stages_ms"]["grouped_w2"]
     out["moe"] = row
-    del g13, g2
     del w13q, w2q, g
 
 
@@ -544,8 +687,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--only-rows", default="",
-                    help="comma list (act_quant,weight_dequant,ragged,prefill_mlp,moe): run just these "
-                         "rows and print them (for profiling)")
+                    help="comma list (decode,act_quant,weight_dequant,ragged,prefill_mlp,moe): run just "
+                         "these rows and print them (for profiling)")
     ap.add_argument("--no-layer-timing", action="store_true",
                     help="skip the per-layer GEMM timing after the timed region (profiling the step alone)")
     ap.add_argument("--ncu-case", default="", choices=[""] + sorted(NCU_CASES),
@@ -578,17 +721,28 @@ def main():
         return
     peaks, peak_src = load_peaks()
     if args.only_rows:
-        print(json.dumps({"rows": rows_measurements(fp8, torch, peaks, set(args.only_rows.split(",")))}),
-              flush=True)
+        only = set(args.only_rows.split(","))
+        dec_rows = Decode(fp8, torch) if "decode" in only else None
+        print(json.dumps({"rows": rows_measurements(fp8, torch, peaks, only, dec=dec_rows)}), flush=True)
         return
     dec = Decode(fp8, torch)
     M = dec.M
 
     # one graph per weight rotation; nothing but the step's kernels, so the
     # programmatic launch edges between consecutive kernels stay intact
+    # one graph holds R consecutive steps (the R weight rotations in turn),
+    # as a decode loop captures many layers in one graph: inside it
+    # consecutive kernels keep their programmatic launch edges.  K steps =
+    # K // R replays of it plus K % R single-step graphs.
+    graph_r = capture(torch, lambda: [dec.step(r) for r in range(dec.R)])
     graphs = [capture(torch, lambda r=r: dec.step(r)) for r in range(dec.R)]
-    for i in range(args.warmup):
-        graphs[i % dec.R].replay()
+
+    def run_steps(n):
+        for _ in range(n // dec.R):
+            graph_r.replay()
+        for i in range(n % dec.R):
+            graphs[i].replay()
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     fp8.fp8_device_status()
 
@@ -601,8 +755,7 @@ def main():
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk.mark("t0")
     t_start.record()
-    for i in range(args.steps):
-        graphs[i % dec.R].replay()
+    run_steps(args.steps)
     t_end.record()
     torch.cuda.synchronize()
     clk.mark("t1")
@@ -630,7 +783,7 @@ def main():
                 wq, wsc = dec.w[r][name]
                 fp8.fp8_linear(dec.x[r][name], wq, wsc, c_bf16=dec.y[name], workspace=dec.ws)
         g = capture(torch, gemms)
-        per_layer[name] = time_graph(torch, g, 50) / dec.R
+        per_layer[name] = time_windows(torch, g, 50)["median"] / dec.R
         del g
     fp8.fp8_device_status()
     dom = max(per_layer, key=per_layer.get) if per_layer else None
@@ -728,7 +881,7 @@ def main():
                                "layer, the quantisation inside the GEMM)",
                    "global_batch": M * world, "parallelism": f"replicas x{world}",
                    "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
-                   "launch": "CUDA graph per step"},
+                   "launch": f"CUDA graphs of {dec.R} steps each (programmatic launch between kernels)"},
         "tflops": world * step_flops / (ms_per_step * 1e9),
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
@@ -751,15 +904,25 @@ def main():
                             "layer_GBps": {n: linear_bytes(M, *syn.DECODE_LAYERS[n]) / v / 1e6
                                            for n, v in per_layer.items()},
                             "timing": "per layer: CUDA graph of its 4 weight-rotation fp8_linear launches, "
-                                      "events around 50 replays, right after the timed region"}
+                                      "median of 5 windows of 50 replays (CUDA events), right after the "
+                                      "timed region"}
     if rank == 0 and world == 1 and not args.no_cpu:
         secs, nb, fl = oracle_decode_sample(torch, dec, 16)
-        line["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": omp_threads(), "kind": "oracle",
+        cores = omp_threads()
+        line["cpu_baseline"] = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": "one decode step: act_quant of all 3 inputs + GEMM over 1/16 of each "
                                           "layer's output features", "seconds": secs}
+        line["cpu_baseline"].update(oracle_gemm_subsets())
+        if _omp_set_threads(1):
+            secs1, nb1, _ = oracle_decode_sample(torch, dec, 64)
+            line["cpu_baseline"]["single_core"] = {
+                "value": nb1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
+                "sample": "one decode step: act_quant of all 3 inputs + GEMM over 1/64 of each layer's "
+                          "output features"}
+            _omp_set_threads(cores)
     if rank == 0 and world == 1 and not args.no_rows:
-        del graphs
-        line["rows"] = rows_measurements(fp8, torch, peaks)
+        del graphs, graph_r
+        line["rows"] = rows_measurements(fp8, torch, peaks, dec=dec)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:
