@@ -478,18 +478,45 @@ def prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=False):
         gemm(xq, xs, w13q, w13s, c_bf16=h13)
         fp8.fp8_silu_mul_quant(h13, h13[:, I:], 2 * I, M, I, fmt, y=gq, s=gsc)
         gemm(gq, gsc, w2q, w2s, c_bf16=yv)
-    g = capture(torch, mlp)
-    t = time_windows(torch, g, 10)
     flops = 3 * gemm_flops(M, I, D)
-    what = ("dense MLP M=4096, 7168->2x18432->7168, " +
-            ("ue8m0 scales on weights and activations, fp8_gemm_ue8m0 (outside config 3, whose weights carry "
-             "fp32 scales)" if ue8m0 else "fp32 scales (config 3), fp8_gemm"))
-    tf = _rate(t, flops, 1e9)
-    # the chain is a 1.1-1.4 ms replay loop: quoted against both the burst and
-    # the sustained (power-capped) dense fp8 peak
-    row = {"workload": what, "ms": t["median"], "ms_min": t["min"], "ms_max": t["max"],
-           "TFLOP/s": tf["median"], "TFLOP/s_min": tf["min"], "TFLOP/s_max": tf["max"],
-           "frac_fp8_peak": tf["median"] / fp8_peak, "frac_fp8_peak_sustained": tf["median"] / fp8_peak_sus}
+
+    def chain_stats(t):
+        tf = _rate(t, flops, 1e9)
+        # the chain is a 1.1-1.4 ms replay loop: quoted against both the burst
+        # and the sustained (power-capped) dense fp8 peak
+        return {"ms": t["median"], "ms_min": t["min"], "ms_max": t["max"],
+                "TFLOP/s": tf["median"], "TFLOP/s_min": tf["min"], "TFLOP/s_max": tf["max"],
+                "frac_fp8_peak": tf["median"] / fp8_peak, "frac_fp8_peak_sustained": tf["median"] / fp8_peak_sus}
+    g = capture(torch, mlp)
+    unfused = chain_stats(time_windows(torch, g, 10))
+    del g
+    if ue8m0:
+        what = ("dense MLP M=4096, 7168->2x18432->7168, ue8m0 scales on weights and activations, "
+                "fp8_gemm_ue8m0 (outside config 3, whose weights carry fp32 scales): act_quant, w1|w3, "
+                "silu*mul+act_quant, w2")
+        row = {"workload": what, **unfused}
+    else:
+        # the production chain: the gate and act_quant in the w1|w3 epilogue
+        # (interleaved weights), then w2 -- three launches
+        w13i = fp8.interleave_w13(w13q[:I], w13q[I:])
+        s13i = fp8.interleave_w13(w13s[: I // 128], w13s[I // 128:], block=1)
+
+        def mlp_fused():
+            fp8.fp8_act_quant(x, fmt, y=xq, s=xs)
+            fp8.fp8_gemm_swiglu(xq, xs, w13i, s13i, fmt, g_q=gq, g_s=gsc)
+            gemm(gq, gsc, w2q, w2s, c_bf16=yv)
+        g = capture(torch, mlp_fused)
+        fused = chain_stats(time_windows(torch, g, 10))
+        del g
+        gsw = capture(torch, lambda: fp8.fp8_gemm_swiglu(xq, xs, w13i, s13i, fmt, g_q=gq, g_s=gsc))
+        tt = time_windows(torch, gsw, 10)
+        r = _rate(tt, gemm_flops(M, 2 * I, D), 1e9)
+        fused["gemm_swiglu"] = {"ms": tt["median"], "TFLOP/s": r["median"], "frac_fp8_peak": r["median"] / fp8_peak,
+                                "frac_fp8_peak_sustained": r["median"] / fp8_peak_sus}
+        del gsw, w13i, s13i
+        what = ("dense MLP M=4096, 7168->2x18432->7168, fp32 scales (config 3): act_quant, fp8_gemm_swiglu "
+                "(w1|w3 with silu*mul+act_quant in its epilogue), fp8_gemm w2")
+        row = {"workload": what, **fused, "unfused_chain": unfused}
     g13 = capture(torch, lambda: gemm(xq, xs, w13q, w13s, c_bf16=h13))
     g2 = capture(torch, lambda: gemm(gq, gsc, w2q, w2s, c_bf16=yv))
     for key, gg, f in (("gemm_w13", g13, gemm_flops(M, 2 * I, D)), ("gemm_w2", g2, gemm_flops(M, D, I))):
@@ -500,7 +527,7 @@ def prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=False):
                     "frac_fp8_peak_sustained": r["median"] / fp8_peak_sus}
     out["prefill_mlp_ue8m0" if ue8m0 else "prefill_mlp"] = row
     del g13, g2
-    del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv, g
+    del w13q, w13s, w2q, w2s, x, xq, xs, h13, gq, gsc, yv
 
 
 def moe_row(fp8, torch, dev, hbm, fp8_peak, out):
@@ -534,15 +561,32 @@ def moe_row(fp8, torch, dev, hbm, fp8_peak, out):
         st.update(off=off, aq=aq, as_=as_, h=h, gq=gq_, gs=gs_, o2=o2)
         st["y"] = fp8.fp8_moe_combine(o2, wts, pr)[0]
     g = capture(torch, moe)
+    t_unfused = time_windows(torch, g, 5)
+    del g
+    # the production chain: gather, w1|w3, gate and act_quant in one grouped
+    # launch (interleaved weights), then w2 and the weighted combine
+    w13i = fp8.interleave_w13(w13q[:, :I], w13q[:, I:])
+    s13i = fp8.interleave_w13(w13s[:, : I // 128], w13s[:, I // 128:], block=1)
+
+    def moe_fused():
+        off, pr, rtok = fp8.fp8_moe_route(ids, E)
+        fp8.fp8_act_quant(x, y=xq, s=xs)
+        gq_, gs_ = fp8.fp8_moe_expert_up(xq, xs, rtok, w13i, s13i, off)
+        o2, _ = fp8.fp8_grouped_gemm(gq_, gs_, w2q, w2s, off)
+        st.update(rtok_f=rtok, off_f=off)
+        st["y_f"] = fp8.fp8_moe_combine(o2, wts, pr)[0]
+    g = capture(torch, moe_fused)
     t = time_windows(torch, g, 5)
     ms = t["median"]
     flops = R * (gemm_flops(1, 2 * I, D) + gemm_flops(1, D, I))
     wbytes = E * (2 * I * D + D * I)
-    row = {"workload": "MoE 4096 tok x top-8 of 256 (Zipf routing), 7168->2x2048->7168", "ms": ms,
-           "ms_min": t["min"], "ms_max": t["max"],
+    row = {"workload": "MoE 4096 tok x top-8 of 256 (Zipf routing), 7168->2x2048->7168: route, act_quant, "
+                       "fp8_moe_expert_up (gather + w1|w3 + silu*mul+act_quant), grouped w2, combine",
+           "ms": ms, "ms_min": t["min"], "ms_max": t["max"],
            "TFLOP/s": flops / ms / 1e9, "weight_GB/s": wbytes / ms / 1e6,
            "roofline_ms": max(wbytes / hbm / 1e6, flops / fp8_peak / 1e9)}
     row["frac_roofline"] = row["roofline_ms"] / ms
+    row["unfused_chain_ms"] = t_unfused["median"]
     # each stage on its own (same inputs as inside the chain)
     stages = {
         "route": lambda: fp8.fp8_moe_route(ids, E),
@@ -553,6 +597,8 @@ def moe_row(fp8, torch, dev, hbm, fp8_peak, out):
                                                          s=st["gs"]),
         "grouped_w2": lambda: fp8.fp8_grouped_gemm(st["gq"], st["gs"], w2q, w2s, st["off"], c_bf16=st["o2"]),
         "combine": lambda: fp8.fp8_moe_combine(st["o2"], wts, st_rt[1]),
+        "expert_up_fused": lambda: fp8.fp8_moe_expert_up(xq, xs, st_rt[2], w13i, s13i, st_rt[0],
+                                                         g_q=st["gq"], g_s=st["gs"]),
     }
     st_rt = fp8.fp8_moe_route(ids, E)
     row["stages_ms"] = {}
@@ -563,7 +609,7 @@ def moe_row(fp8, torch, dev, hbm, fp8_peak, out):
     row["grouped_w13_ms"] = row["stages_ms"]["grouped_w13"]
     row["grouped_w2_ms"] = row["stages_ms"]["grouped_w2"]
     out["moe"] = row
-    del w13q, w2q, g
+    del w13q, w2q, g, w13i, s13i
 
 
 # ------------------------------------------------------------------ reference arm

@@ -53,6 +53,9 @@ def _declare(lib):
         "fp8_linear_workspace_size": (sz, [i64, i64, i64]),
         "fp8_linear": (st, [vp, vp, f32p, vp, f32p, i64, i64, i64, ctypes.c_int, vp, sz, vp]),
         "fp8_gemm_noalloc": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, vp]),
+        "fp8_gemm_swiglu": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, ctypes.c_int, vp]),
+        "fp8_moe_expert_up": (st, [vp, f32p, i64, vp, vp, f32p, vp, i32, i64, vp, f32p, i64, i64, ctypes.c_int,
+                                   vp]),
         "fp8_debug_set_wait_limit": (st, [ctypes.c_longlong]),
         "fp8_debug_skip_one_arrive": (None, []),
         "fp8_device_status": (st, [vp]),
@@ -276,6 +279,69 @@ def fp8_grouped_gemm(a, a_s, b, b_s, offsets, out_bf16=True, out_fp32=False, c_b
     _check("fp8_grouped_gemm", lib.fp8_grouped_gemm(_ptr(a), _ptr(a_s), _ptr(b), _ptr(b_s), _ptr(offsets),
                                                     G, R, _ptr(c_bf16), _ptr(c_fp32), N, K, _stream(stream)))
     return c_bf16, c_fp32
+
+
+def interleave_w13(w1, w3, block=BLOCK):
+    """Lay w1 and w3 ([I, K] each, or [G, I, K]) out as the fused kernels
+    expect: 128-row blocks alternating w1, w3 -> [2I, K] (or [G, 2I, K]).
+    Also for their scale grids ([I/128, K/128] -> [2I/128, K/128]) with
+    block=1.  Pure data layout (a copy), no arithmetic."""
+    if w1.shape != w3.shape:
+        raise ValueError("w1 and w3 differ in shape")
+    *lead, I, K = w1.shape
+    if I % block:
+        raise ValueError("rows not a multiple of the block")
+    nb = I // block
+    dt = w1.dtype
+    if dt == torch.float8_e4m3fn:   # (moved as bytes)
+        w1, w3 = w1.view(torch.uint8), w3.view(torch.uint8)
+    a = w1.reshape(*lead, nb, block, K)
+    b = w3.reshape(*lead, nb, block, K)
+    return torch.stack([a, b], dim=-3).reshape(*lead, 2 * I, K).contiguous().view(dt)
+
+
+def fp8_gemm_swiglu(a, a_s, w13, w13_s, scale_fmt=FP8_SCALE_FP32, g_q=None, g_s=None, stream=None):
+    """act_quant(bf16(silu(h1)) * h3) with h1|h3 = a @ w13^T (w13 interleaved,
+    see interleave_w13), in one GEMM launch.  Returns (g_q [M, I] e4m3,
+    g_s [M, I/128] fp32)."""
+    _cuda(a, "a", _E4M3, 2)
+    _cuda(w13, "w13", _E4M3, 2)
+    _cuda(a_s, "a_s", _F32, 2)
+    _cuda(w13_s, "w13_s", _F32, 2)
+    M, K = a.shape
+    I = w13.shape[0] // 2
+    if w13.shape[1] != K or tuple(w13_s.shape) != (2 * I // BLOCK, K // BLOCK):
+        raise ValueError("shape mismatch")
+    g_q = _empty_e4m3((M, I), a.device) if g_q is None else _cuda(g_q, "g_q", _E4M3)
+    g_s = torch.empty((M, I // BLOCK), dtype=torch.float32, device=a.device) if g_s is None else _cuda(g_s, "g_s", _F32)
+    _check("fp8_gemm_swiglu", lib.fp8_gemm_swiglu(_ptr(a), _ptr(a_s), _ptr(w13), _ptr(w13_s), _ptr(g_q), _ptr(g_s),
+                                                  M, I, K, int(scale_fmt), _stream(stream)))
+    return g_q, g_s
+
+
+def fp8_moe_expert_up(xq, xs, row_token, w13, w13_s, offsets, scale_fmt=FP8_SCALE_FP32, g_q=None, g_s=None,
+                      stream=None):
+    """Gather + grouped w1|w3 + silu*mul + act_quant in one launch.  xq [T, K]
+    e4m3 / xs [T, K/128]; row_token int32 [R]; w13 [G, 2I, K] interleaved;
+    offsets int32 [G+1].  Returns (g_q [R, I], g_s [R, I/128])."""
+    _cuda(xq, "xq", _E4M3, 2)
+    _cuda(xs, "xs", _F32, 2)
+    _cuda(row_token, "row_token", _I32, 1)
+    _cuda(w13, "w13", _E4M3, 3)
+    _cuda(w13_s, "w13_s", _F32, 3)
+    _cuda(offsets, "offsets", _I32, 1)
+    T, K = xq.shape
+    G, N2, Kw = w13.shape
+    I = N2 // 2
+    R = row_token.numel()
+    if Kw != K or offsets.numel() != G + 1:
+        raise ValueError("shape mismatch")
+    g_q = _empty_e4m3((R, I), xq.device) if g_q is None else g_q
+    g_s = torch.empty((R, I // BLOCK), dtype=torch.float32, device=xq.device) if g_s is None else g_s
+    _check("fp8_moe_expert_up", lib.fp8_moe_expert_up(_ptr(xq), _ptr(xs), T, _ptr(row_token), _ptr(w13), _ptr(w13_s),
+                                                      _ptr(offsets), G, R, _ptr(g_q), _ptr(g_s), I, K,
+                                                      int(scale_fmt), _stream(stream)))
+    return g_q, g_s
 
 
 def fp8_silu_mul_quant(h1, h3, ld_h, R, I, scale_fmt=FP8_SCALE_FP32, want_g=False, y=None, s=None,

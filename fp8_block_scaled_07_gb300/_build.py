@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libfp8bs.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "moe.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "decode.cu", "moe.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(ROOT, "include", "fp8bs.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -4,7 +4,8 @@
 
 namespace fp8bs {
 
-int gemm_read_and_clear_status(cudaStream_t st);   // gemm.cu
+int gemm_read_and_clear_status(cudaStream_t st);     // gemm.cu
+int decode_read_and_clear_status(cudaStream_t st);   // decode.cu
 
 int device_sm_count() {
     static int cache[64] = {0};
@@ -31,8 +32,10 @@ extern "C" fp8_status fp8_device_status(void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return FP8_ERR_CUDA;
     const int v = gemm_read_and_clear_status(st);
-    if (v < 0) return FP8_ERR_CUDA;
-    return v == 0 ? FP8_OK : static_cast<fp8_status>(v);
+    const int d = decode_read_and_clear_status(st);
+    if (v < 0 || d < 0) return FP8_ERR_CUDA;
+    if (v != 0) return static_cast<fp8_status>(v);
+    return d == 0 ? FP8_OK : static_cast<fp8_status>(d);
 }
 
 extern "C" const char* fp8_status_string(fp8_status status) {

@@ -10,6 +10,7 @@
 
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -161,6 +162,21 @@ __device__ __forceinline__ void unpack_bf16x8_neg(const uint4& v, float (&nx)[8]
     }
 }
 
+// The expert body's gate for one element pair: g = bf16(bf16(silu(h1)) * h3)
+// with silu(v) = v / (1 + exp(-v)) in fp32, from bf16 inputs given as fp32
+// (exact).  The one routine of the library for it: the standalone
+// silu*mul+act_quant kernel and the GEMM epilogues that fuse it both call
+// it, so their results agree bit for bit.  Returns the two bf16 results
+// packed (first in the low half).
+__device__ __forceinline__ uint32_t silu_mul_bf16x2(float a0, float a1, float b0, float b1) {
+    const float s0 = a0 / (1.0f + expf(-a0));
+    const float s1 = a1 / (1.0f + expf(-a1));
+    const float sb0 = __bfloat162float(__float2bfloat16_rn(s0));
+    const float sb1 = __bfloat162float(__float2bfloat16_rn(s1));
+    const __nv_bfloat162 g = __floats2bfloat162_rn(sb0 * b0, sb1 * b1);
+    return *reinterpret_cast<const uint32_t*>(&g);
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the
 // async proxy (the tensor core reading operands from shared memory).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -232,6 +248,18 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
         : "memory");
 }
 
+// Row gather: four rows (y0..y3) of a 2-D tensor, each one box wide starting
+// at column x, into four consecutive rows of shared memory (the tensor map's
+// box is one row high); completion counted on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* tmap, uint64_t* bar,
                                                  int32_t x, int32_t y, uint64_t policy) {
     asm volatile(
@@ -259,6 +287,12 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -407,6 +441,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+          "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+          "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+          "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
         : "r"(taddr));
 }
 
@@ -566,6 +619,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// L2 prefetch of the cache line holding `p` (non-binding, no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // L2 prefetch of one TMA box (no shared memory involved).  L2 is the point
 // of coherence, so prefetching before griddep_wait() cannot expose stale
 // data to the loads that follow it.
@@ -613,5 +671,15 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 int device_sm_count();   // cached per device (api.cu)
+
+// Batches the decode kernel (decode.cu) serves: fp8_gemm up to 64 tokens;
+// fp8_linear quantises the activations inside it up to 16 tokens.
+constexpr int64_t kDecodeMaxM = 64;
+constexpr int64_t kDecodeFusedMaxM = 16;
+
+// TMA tensor maps over row-major matrices [rows, K], 128-byte swizzle (gemm.cu):
+// e4m3 with boxes of 128 x box_rows bytes; bf16 with boxes of 64 x box_rows.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows);
+bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows);
 
 }  // namespace fp8bs

@@ -19,9 +19,8 @@
 //     registers ("promotion"), while the tensor core fills the other slab
 //     buffer;
 //   * warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
-//     owner), warps 4..7 = epilogue; persistent CTAs, one per SM;
-//   * decode shapes (M <= 64) swap the operands: the weight fills the
-//     128-row MMA side and the tokens the N side (16..64);
+//     owner), warps 4.. = epilogue; persistent CTAs, one per SM;
+//   * decode shapes (M <= 64) run on the kernel of decode.cu instead;
 //   * few tiles -> stream-K: each CTA takes an equal run of (tile, slab)
 //     units; tiles split across CTAs are reduced deterministically by the
 //     CTA that finishes a tile last (fp32 partials in the caller's
@@ -81,12 +80,19 @@ constexpr int kMaxGroups = 1024;
 constexpr int kMaxSkTiles = 4096;
 constexpr size_t kCounterBytes = kMaxSkTiles * sizeof(int);
 
-enum Variant { kDense = 0, kDenseSwap = 1, kGrouped = 2, kSwapFused = 3 };
-// swapped layout (weights on the 128-row MMA side); kSwapFused also
-// quantises the bf16 activations inside the kernel (act_quant fused)
-template <int V>
-constexpr bool is_swap() { return V == kDenseSwap || V == kSwapFused; }
-constexpr int kScaleChunk = 32;   // slabs of scale products staged at a time (swapped layout)
+enum Variant { kDense = 0, kGrouped = 2 };
+
+// Register split of the 128x256 kernels (warpgroup 0 / epilogue warpgroups)
+// and the width of the epilogue's TMEM loads (columns per tcgen05.ld).
+#ifndef FP8BS_REGS_LOW
+#define FP8BS_REGS_LOW 120
+#endif
+#ifndef FP8BS_REGS_HIGH
+#define FP8BS_REGS_HIGH 192
+#endif
+#ifndef FP8BS_EPI_LD
+#define FP8BS_EPI_LD 32
+#endif
 
 struct Params {
     const float* a_s;          // [rows_a, KB]
@@ -106,13 +112,20 @@ struct Params {
     int stream_k;              // 1: stream-K schedule over total_units
     long long total_units;     // num_tiles * KB
     int trace_slot;            // profiling builds: which timeline buffer this launch fills
-    int ksplit;                // >0: cluster split-K, CTA = (tile, K part), cluster of ksplit CTAs
-    const uint16_t* x;         // fused: bf16 activations [M, K]
-    long long K;               // fused: row stride of x
-    int ue8m0;                 // fused: activation scale format
     int tma_store;             // dense, bf16 only: full tiles leave through shared memory and TMA
     int vec_scales;            // scale rows are 16-byte aligned (K/128 % 4 == 0, aligned bases)
     int debug_skip;            // test hook: the MMA issuer skips its arrive on slab 0's TMEM-full barrier
+    // expert body fused into the epilogue of the w1|w3 product (128x256 tiles;
+    // weights interleaved so a tile holds h1 and h3 of one 128-wide block):
+    // g = bf16(bf16(silu(h1)) * h3) -> act_quant -> gq [rows, N/2] e4m3,
+    // gs [rows, N/256] fp32, instead of storing h
+    int swiglu;
+    int ue8m0;                 // swiglu: scale format of g's codes
+    uint8_t* gq;
+    float* gs;
+    // grouped: A rows gathered from the token rows row_token[r] of a [T, K]
+    // matrix (the producer's TMA row gather) instead of read packed
+    const int32_t* row_token;
 };
 
 struct Tile {
@@ -128,48 +141,34 @@ struct Seg {
 
 template <int BN, int V>
 struct Cfg {
-    static constexpr bool kFusedV = (V == kSwapFused);
-    static constexpr bool kSwap = is_swap<V>();
-    static constexpr bool kFused = kFusedV;
     static constexpr int kQTileBytes = BN * kBlock;
-    static constexpr int kXTileBytes = kFusedV ? BN * kBlock * 2 : 0;   // fused: bf16 activation tile
-    static constexpr int kStageBytes = kPTileBytes + kQTileBytes + kXTileBytes;
-    // small swapped tiles: 5 stages (80 KB of weights in flight) so that two
-    // CTAs fit on an SM -- the next launch's CTAs start while this one drains
-    static constexpr int kStages = kFusedV ? 4 : ((kSwap && BN <= 32) ? 5 : (BN == 256 ? 4 : (BN >= 128 ? 6 : 7)));
-    static constexpr int kMinBlocks = (kSwap && BN <= 32) ? 2 : 1;
+    static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
+    static constexpr int kStages = BN == 256 ? 4 : 6;
     // 128x256 tiles: 8 epilogue warps, two per TMEM lane quarter, each owning
     // 128 of the 256 columns; their warpgroups take registers from warps 0-3
     static constexpr int kEpiWarps = BN == 256 ? 8 : 4;
-    // fused: two more quantiser warps after the epilogue (four in all)
-    static constexpr int kQuantWarps = kFusedV ? 4 : 0;
-    static constexpr int kThreads = 128 + 32 * kEpiWarps + (kFusedV ? 64 : 0);
+    static constexpr int kThreads = 128 + 32 * kEpiWarps;
+    static constexpr int kMinBlocks = 1;
     static constexpr int kCPT = BN * 4 / kEpiWarps;   // accumulator columns per epilogue thread
     static constexpr bool kSplitRegs = kEpiWarps == 8;
-    // dense / grouped: the MMA issuer checks one barrier per slab (each check
-    // by the issuing thread costs tensor time): a stage's full barrier also
-    // counts the epilogue warps' release of the TMEM buffer the slab will
-    // write, i.e. of the slab two before it
-    static constexpr bool kMergeT = V == kDense || V == kGrouped;
+    // the MMA issuer checks one barrier per slab (each check by the issuing
+    // thread costs tensor time): a stage's full barrier also counts the
+    // epilogue warps' release of the TMEM buffer the slab will write, i.e. of
+    // the slab two before it
+    static constexpr bool kMergeT = true;
     // the producer and MMA warps keep their tile state in registers (spills
     // there were reloaded every slab); 120*128 + 192*256 = 168*384
-    static constexpr int kRegsLow = 120, kRegsHigh = 192;
-    static constexpr int kTmemCols = (2 * BN) < 32 ? 32 : 2 * BN;   // power of two for BN in {16,...,256}
+    static constexpr int kRegsLow = FP8BS_REGS_LOW, kRegsHigh = FP8BS_REGS_HIGH;
+    static constexpr int kTmemCols = 2 * BN;   // two slab buffers
     static constexpr int kBarBytes = 1024;
-    // grouped: per-expert tile prefix; swapped: two chunks of staged scales
-    // swapped: staged scales + the split-K receive buffer (128 x BN fp32)
-    static constexpr int kRecvBytes = kSwap ? 128 * BN * 4 : 0;
-    // fused: ring of per-slab scale products handed from quantiser to epilogue
-    static constexpr int kRingSlots = kStages + 2;
-    static constexpr int kExtraBytes =
-        V == kGrouped ? (kMaxGroups + 1 + 16) * 4
-                      : (kSwap ? 2 * kScaleChunk * BN * 4 + kRecvBytes + (kFused ? kRingSlots * BN * 4 : 0) : 0);
-    // dense / grouped: per epilogue warp a staging box (kStgRows rows x 64
-    // bf16, 128-byte swizzle) through which output tiles leave by TMA stores;
-    // 32 rows dense, 16 grouped (whose expert-tile prefix takes the room)
-    static constexpr bool kTmaStore = V == kDense || V == kGrouped;
+    // grouped: per-expert tile prefix
+    static constexpr int kExtraBytes = V == kGrouped ? (kMaxGroups + 1 + 16) * 4 : 0;
+    // per epilogue warp a staging box (kStgRows rows x 64 bf16, 128-byte
+    // swizzle) through which output tiles leave by TMA stores; 32 rows dense,
+    // 16 grouped (whose expert-tile prefix takes the room)
+    static constexpr bool kTmaStore = true;
     static constexpr int kStgRows = V == kGrouped ? 16 : 32;
-    static constexpr int kStgBytes = kTmaStore ? kEpiWarps * kStgRows * 128 : 0;
+    static constexpr int kStgBytes = kEpiWarps * kStgRows * 128;
     static constexpr int kSmemBytes =
         1024 /*align slack*/ + kStages * kStageBytes + kStgBytes + kBarBytes + kExtraBytes;
     // weight slabs each CTA prefetches into L2 before its inputs are ready
@@ -191,20 +190,12 @@ struct SegIter {
     // data-parallel: tiles blockIdx.x + i * gridDim.x; stream-K: units [lo, hi)
     long long u, hi;
     int t, stride, num_tiles, KB;
-    int cl_tile, cl_k0, cl_k1;
-    bool sk, cl = false, cl_done = false;
+    bool sk;
     __device__ void init(const Params& p, int ntiles) {
         KB = p.KB;
         sk = p.stream_k != 0;
         num_tiles = ntiles;
-        if (p.ksplit > 0) {   // one segment: K part (blockIdx % c) of tile (blockIdx / c)
-            const unsigned c = static_cast<unsigned>(p.ksplit), b = blockIdx.x;
-            const unsigned t0 = b / c, part = b - t0 * c, kb = static_cast<unsigned>(KB);
-            cl_tile = static_cast<int>(t0);
-            cl_k0 = static_cast<int>(part * kb / c);
-            cl_k1 = static_cast<int>((part + 1) * kb / c);
-            cl = true;
-        } else if (sk) {
+        if (sk) {
             u = sk_start(blockIdx.x, p.total_units, gridDim.x);
             hi = sk_start(blockIdx.x + 1, p.total_units, gridDim.x);
         } else {
@@ -213,14 +204,6 @@ struct SegIter {
         }
     }
     __device__ bool next(Seg& s) {
-        if (cl) {
-            if (cl_done) return false;
-            s.tile = cl_tile;
-            s.k0 = cl_k0;
-            s.k1 = cl_k1;
-            cl_done = true;
-            return true;
-        }
         if (sk) {
             if (u >= hi) return false;
             s.tile = static_cast<int>(u / KB);
@@ -272,12 +255,6 @@ __device__ __forceinline__ Tile tile_geom(const Params& p, int t, const int* s_p
         g.q_row0 = tq * BN;
         g.p_valid = min(128, p.M - g.p_row0);
         g.q_valid = min(BN, p.N - g.q_row0);
-    } else if (is_swap<V>()) {
-        const int tp = t % p.tiles_p, tq = t / p.tiles_p;
-        g.p_row0 = tp * 128;         // weight rows (output columns)
-        g.q_row0 = tq * BN;          // token rows
-        g.p_valid = min(128, p.N - g.p_row0);
-        g.q_valid = min(BN, p.M - g.q_row0);
     } else {
         int lo = 0, hi = p.G;        // largest g with s_prefix[g] <= t
         while (hi - lo > 1) {
@@ -308,24 +285,10 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
 // of a bounded wait is made warp-uniform before any warp-collective step.
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xFFFFFFFFu, ok) != 0; }
 
-// Store the CPT accumulators of one output row starting at tile column
-// cofs (non-swapped layout) or of one output column (swapped layout).
+// Store the CPT accumulators of one output row starting at tile column cofs.
 template <int BN, int V, int CPT>
 __device__ __forceinline__ void store_tile(const Params& p, const Tile& tg, int e, int cofs,
                                            const float (&acc)[CPT]) {
-    if (is_swap<V>()) {
-        const int n = tg.p_row0 + e;
-        if (e >= tg.p_valid) return;
-#pragma unroll
-        for (int j = 0; j < BN; ++j) {
-            if (j < tg.q_valid) {
-                const int64_t idx = static_cast<int64_t>(tg.q_row0 + j) * p.N + n;
-                if (p.c_bf16) p.c_bf16[idx] = __float2bfloat16_rn(acc[j]);
-                if (p.c_fp32) p.c_fp32[idx] = acc[j];
-            }
-        }
-        return;
-    }
     if (e >= tg.p_valid) return;
     const int64_t row = tg.p_row0 + e;
     const int col0 = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) + cofs;
@@ -411,68 +374,104 @@ __device__ __forceinline__ int store_tile_tma(const CUtensorMap* tm_c, uint8_t* 
     return 32;
 }
 
-// Fused act_quant for the swapped decode layout (BN == 16): four quantiser
-// warps (2-3 and the two after the epilogue warps), 128 threads; thread
-// (r, sub) quantises values [16 sub, 16 sub + 16) of token row r of each
-// slab from the bf16 tile TMA placed in shared memory (two 64-column halves,
-// 128-byte swizzle); the eight threads of a row share the block max by
-// shuffles.  Codes go to the stage's e4m3 tile in the layout the MMA reads;
-// the scale products b_s * a_s go to a ring the epilogue reads.
-template <int BN, int S>
-__device__ __forceinline__ void quantiser_role(const Params& p, SegIter it, const int* s_prefix, uint8_t* sQ,
-                                               const uint8_t* sX, float* s_ring, uint64_t* full, uint64_t* xfull,
-                                               volatile int* abort_flag) {
-    static_assert(BN == 16, "fused quantisation covers 16-token tiles");
-    constexpr int kQTile = BN * kBlock, kXTile = BN * kBlock * 2, kRing = S + 2;
-    const int t = static_cast<int>(threadIdx.x);
-    const int qt = t < 128 ? t - 64 : t - 256 + 64;   // 0..127 over warps 2-3, 8-9
-    const int lane = t & 31;
-    const int r = qt >> 3, sub = qt & 7;
-    uint32_t iter = 0;
-    Seg sg;
-    griddep_wait();
-    while (it.next(sg)) {
-        const Tile tg = tile_geom<BN, kSwapFused>(p, sg.tile, s_prefix);
-        const bool valid = r < tg.q_valid;
-        const float* bs_row = p.b_s + static_cast<int64_t>(tg.p_row0 / 128) * p.KB;
-        float bsc = __ldg(bs_row + sg.k0);
-        for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
-            const float bsc_next = kb + 1 < sg.k1 ? __ldg(bs_row + kb + 1) : 0.0f;
-            const int st = iter % S;
-            if (!warp_all(mbar_wait(&xfull[st], (iter / S) & 1, abort_flag))) {
-                set_abort(abort_flag);
-                return;
-            }
-            // columns [16 sub, 16 sub + 16): half sub / 4, chunks 2 (sub % 4) and +1
-            const uint8_t* xrow = sX + st * kXTile + (sub >> 2) * (kXTile / 2) + r * 128;
-            float nx[2][8];   // the values negated, as quant8n takes them
+// The expert body fused into the epilogue of a 128x256 tile of the w1|w3
+// product ("Behavior traces", bullet "MoE trace": each expert computes
+// w2(silu(w1 x) * w3 x); source tour, "FP8 with per-block scales": the
+// input of w2 is quantised per 128 block).  The weights are interleaved so
+// that tile columns 0-127 are h1 = x w1^T and 128-255 are h3 = x w3^T of the
+// same 128-wide block of the intermediate dimension.  The two epilogue warps
+// of a TMEM lane quarter (half 0: h1, half 1: h3, the same 32 rows) swap
+// halves through their staging boxes (ROWS rows at a time): half 0 then
+// makes g for columns 0-63, half 1 for columns 64-127, with the library's
+// silu*mul routine on the bf16-rounded h values (what the GEMM would have
+// stored); the row's block max is combined through the boxes too, and each
+// warp quantises its 64 values with act_quant's routine and stores their
+// codes, half 0 also the row's scale.  Bit-identical to storing h in bf16
+// and running the standalone silu*mul+act_quant on it.
+template <int ROWS>
+__device__ __forceinline__ void swiglu_quant_epilogue(const Params& p, uint8_t* my_box, const uint8_t* peer_box,
+                                                      int half, int lane, int q, bool row_valid, int64_t out_row,
+                                                      int iblk, const float (&acc)[128]) {
+    // bf16 pairs of the 64 values this warp keeps (half 0: h1[0:64], half 1:
+    // h3[64:128]) and of the 64 it gives away (h1[64:128], h3[0:64]); the
+    // accumulators are dead after this loop (constant indices in both
+    // branches keep them in registers)
+    uint32_t keep[32], give[32], recv[32];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int c = (sub & 3) * 2 + i;
-                unpack_bf16x8_neg(*reinterpret_cast<const uint4*>(xrow + ((c ^ (r & 7)) * 16)), nx[i]);
-            }
-            float amax = fmaxf(max_abs8(nx[0]), max_abs8(nx[1]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-            const float sc = block_scale(amax, p.ue8m0 != 0);
-            const float rc = __frcp_rn(sc);
-            uint2 q[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                q[i] = p.ue8m0 ? quant8n<true>(nx[i], sc, rc) : quant8n<false>(nx[i], sc, rc);
-                if (!valid) q[i] = make_uint2(0, 0);
-            }
-            // 16-byte e4m3 chunk sub of row r, 128-byte swizzle
-            uint8_t* row = sQ + st * kQTile + r * 128;
-            *reinterpret_cast<uint4*>(row + ((sub ^ (r & 7)) * 16)) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
-            if (sub == 0) s_ring[(iter % kRing) * BN + r] = valid ? bsc * sc : 0.0f;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[st]);
-            bsc = bsc_next;
-        }
+    for (int j = 0; j < 32; ++j) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[64 + 2 * j], acc[64 + 2 * j + 1]);
+        const uint32_t ulo = *reinterpret_cast<const uint32_t*>(&lo), uhi = *reinterpret_cast<const uint32_t*>(&hi);
+        keep[j] = half == 0 ? ulo : uhi;
+        give[j] = half == 0 ? uhi : ulo;
     }
+#pragma unroll
+    for (int r0 = 0; r0 < 32; r0 += ROWS) {
+        const bool mine = lane >= r0 && lane < r0 + ROWS;
+        const int row = lane - r0;
+        if (mine) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(my_box + row * 128 + ((c ^ (row & 7)) * 16)) =
+                    make_uint4(give[4 * c], give[4 * c + 1], give[4 * c + 2], give[4 * c + 3]);
+        }
+        named_bar_sync(1 + q, 64);
+        if (mine) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(peer_box + row * 128 + ((c ^ (row & 7)) * 16));
+                recv[4 * c] = v.x;
+                recv[4 * c + 1] = v.y;
+                recv[4 * c + 2] = v.z;
+                recv[4 * c + 3] = v.w;
+            }
+        }
+        named_bar_sync(1 + q, 64);   // both read before the boxes are written again
+    }
+    // g of this warp's 64 columns, packed bf16 pairs
+    uint32_t g[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t u1 = half == 0 ? keep[j] : recv[j];   // h1 pair
+        const uint32_t u3 = half == 0 ? recv[j] : keep[j];   // h3 pair
+        g[j] = silu_mul_bf16x2(__uint_as_float(u1 << 16), __uint_as_float(u1 & 0xFFFF0000u),
+                               __uint_as_float(u3 << 16), __uint_as_float(u3 & 0xFFFF0000u));
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(g[j] << 16)), fabsf(__uint_as_float(g[j] & 0xFFFF0000u))));
+    }
+    // the row's block max over both halves
+    float peer_amax = 0.0f;
+#pragma unroll
+    for (int r0 = 0; r0 < 32; r0 += ROWS) {
+        const bool mine = lane >= r0 && lane < r0 + ROWS;
+        const int row = lane - r0;
+        if (mine) *reinterpret_cast<float*>(my_box + row * 128) = amax;
+        named_bar_sync(1 + q, 64);
+        if (mine) peer_amax = *reinterpret_cast<const float*>(peer_box + row * 128);
+        named_bar_sync(1 + q, 64);
+    }
+    amax = fmaxf(amax, peer_amax);
+    const float sc = block_scale(amax, p.ue8m0 != 0);
+    if (!row_valid) return;
+    const int I = p.N / 2;
+    uint4* dst = reinterpret_cast<uint4*>(p.gq + out_row * I + iblk * 128 + half * 64);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint2 qv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float f[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w = g[8 * c + 4 * h + u];
+                f[2 * u] = __uint_as_float(w << 16);
+                f[2 * u + 1] = __uint_as_float(w & 0xFFFF0000u);
+            }
+            qv[h] = p.ue8m0 ? quant8<true>(f, sc) : quant8<false>(f, sc);
+        }
+        dst[c] = make_uint4(qv[0].x, qv[0].y, qv[1].x, qv[1].y);
+    }
+    if (half == 0) p.gs[out_row * (I / 128) + iblk] = sc;
 }
 
 // Exclusive prefix over experts of their tile counts (m-tiles x tq), by the
@@ -543,6 +542,14 @@ __device__ __forceinline__ void promote(uint32_t taddr, float (&acc)[BN], const 
         tmem_ld16(taddr, r);
         tmem_wait_ld();
         fma_chunk<16, PER_COL>(acc, r, sc_col, sc);
+    } else if constexpr (FP8BS_EPI_LD == 64 && BN % 64 == 0) {
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+            uint32_t r[64];
+            tmem_ld64(taddr + c0, r);
+            tmem_wait_ld();
+            fma_chunk<64, PER_COL>(acc + c0, r, PER_COL ? sc_col + c0 : nullptr, sc);
+        }
     } else {
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -579,8 +586,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sP = smem;                                   // S x 16 KB
     uint8_t* sQ = smem + S * kPTileBytes;                 // S x BN*128
-    uint8_t* sX = sQ + S * C::kQTileBytes;                // fused: S x (BN x 128 bf16, two swizzled halves)
-    uint8_t* sStg = smem + S * C::kStageBytes;           // dense: kEpiWarps x 4 KB output staging
+    uint8_t* sStg = smem + S * C::kStageBytes;           // kEpiWarps output staging boxes
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes + C::kStgBytes);
     uint64_t* full = bars;                 // S
     uint64_t* empty = bars + S;            // S
@@ -588,15 +594,10 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     uint64_t* tempty = bars + 2 * S + 2;   // 2
     uint64_t* mma_done = bars + 2 * S + 4; // 1
     uint64_t* epi_bar = bars + 2 * S + 5;  // epilogue-group barrier
-    uint64_t* red_bar = bars + 2 * S + 6;  // cluster split-K: all partials pushed to this CTA
-    uint64_t* xfull = bars + 2 * S + 8;    // fused: S barriers, activation tile landed
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 8);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
     int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kStgBytes + C::kBarBytes);
-    float* s_scale = reinterpret_cast<float*>(smem + S * C::kStageBytes + C::kStgBytes + C::kBarBytes);
-    float* s_recv = s_scale + 2 * kScaleChunk * BN;   // swapped: split-K partials pushed here
-    float* s_ring = s_recv + 128 * BN;                 // fused: per-slab scale products
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -604,10 +605,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            // fused: TMA + the quantiser warps; dense / grouped: TMA + the epilogue warps
-            mbar_init(&full[i], C::kFused ? 1 + C::kQuantWarps : (C::kMergeT ? 1 + C::kEpiWarps : 1));
+            // the producer's bytes + the epilogue warps' release of a TMEM buffer
+            mbar_init(&full[i], 1 + C::kEpiWarps);
             mbar_init(&empty[i], 1);
-            if (C::kFused) mbar_init(&xfull[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -622,7 +622,6 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         }
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
-        mbar_init(red_bar, 1);   // cluster split-K: the owner's own arrival + the pushed bytes
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -638,10 +637,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             int n = 0;
             while (n < C::kL2Prefetch && pit.next(ps)) {
                 const Tile tg = tile_geom<BN, V>(p, ps.tile, nullptr);
-                for (int kb = ps.k0; kb < ps.k1 && n < C::kL2Prefetch; ++kb, ++n) {
-                    if (is_swap<V>()) tma_prefetch_l2_2d(&tm_p, kb * kBlock, tg.p_row0);
-                    else tma_prefetch_l2_2d(&tm_q, kb * kBlock, tg.q_row0);
-                }
+                for (int kb = ps.k0; kb < ps.k1 && n < C::kL2Prefetch; ++kb, ++n)
+                    tma_prefetch_l2_2d(&tm_q, kb * kBlock, tg.q_row0);
             }
         }
     }
@@ -653,9 +650,6 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // every CTA of a split-K cluster has initialised its barriers before any
-    // of them may arrive on a remote one
-    if (p.ksplit > 1) cluster_sync_all();
     // dependents may launch only once this CTA holds its tensor memory (a
     // dependent CTA on the same SM must never take columns this one needs);
     // an otherwise idle warp signals, so the producer is not delayed
@@ -663,8 +657,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     // Inputs written by earlier launches are visible to a thread once it has
     // passed griddepcontrol.wait.  Each role waits just before its first
     // access to global memory, so the set-up before it overlaps the previous
-    // launch: the producer before its first load, the quantiser and the
-    // epilogue before their first scale load; the MMA issuer touches only
+    // launch: the producer before its first load, the epilogue before its
+    // first scale load; the MMA issuer touches only
     // shared and tensor memory.  The grouped kernel's tile prefix reads the
     // offsets with the whole block, so it waits here.
     if constexpr (V == kGrouped) griddep_wait();
@@ -687,7 +681,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
+        // (gathered A rows: the whole warp, one 4-row TMA gather per lane)
+        const bool gather = (V == kGrouped) && p.row_token != nullptr;
+        if (gather || lane == 0) {
             uint32_t iter = 0;
             bool ok = true;
 #ifdef FP8BS_TRACE_ENABLED
@@ -695,11 +691,22 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 #endif
             while (ok && it.next(sg)) {
                 const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
+                // token rows of tile rows 4 lane .. 4 lane + 3 (rows past the
+                // expert's last repeat a valid one; their results are not stored)
+                int tok[4] = {0, 0, 0, 0};
+                if (gather) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        tok[i] = __ldg(p.row_token + tg.p_row0 + min(4 * lane + i, tg.p_valid - 1));
+                }
                 for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
                     const int st = iter % S;
                     FP8BS_TIC(t0_);
-                    if (!mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag)) {
-                        set_abort(abort_flag);
+                    bool free_st = true;
+                    if (lane == 0) free_st = mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag);
+                    if (gather) free_st = __shfl_sync(0xFFFFFFFFu, free_st ? 1 : 0, 0) != 0;
+                    if (!free_st) {
+                        if (lane == 0) set_abort(abort_flag);
                         ok = false;
                         break;
                     }
@@ -709,16 +716,13 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                         FP8BS_TRACE(8);
                         FP8BS_TRACE(2);
                     }
-                    if constexpr (C::kFused) {
-                        // activation tile (two 64-column halves) for the quantiser
-                        mbar_arrive_expect_tx(&xfull[st], C::kXTileBytes);
-                        tma_load_2d(sX + st * C::kXTileBytes, &tm_q, &xfull[st], kb * kBlock, tg.q_row0);
-                        tma_load_2d(sX + st * C::kXTileBytes + C::kXTileBytes / 2, &tm_q, &xfull[st],
-                                    kb * kBlock + 64, tg.q_row0);
-                        mbar_arrive_expect_tx(&full[st], kPTileBytes);
-                        tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
+                    if (lane == 0) mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                    if (gather) {
+                        __syncwarp();
+                        tma_gather4(sP + st * kPTileBytes + lane * 4 * 128, &tm_p, &full[st], kb * kBlock, tok[0],
+                                    tok[1], tok[2], tok[3]);
+                        if (lane == 0) tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
                     } else {
-                        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
                         tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
                         tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
                     }
@@ -726,10 +730,12 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             }
             FP8BS_TRACE_VAL(11, static_cast<unsigned long long>(w_empty));
             // drain: every load issued must land before the CTA may exit
-            for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
-                const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
-                const volatile int never = 0;
-                if (!mbar_wait(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
+            if (lane == 0) {
+                for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
+                    const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
+                    const volatile int never = 0;
+                    if (!mbar_wait(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
+                }
             }
         }
     } else if (warp == 1) {
@@ -746,13 +752,12 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                     const int st = iter % S;
                     const int buf = slab & 1;
                     FP8BS_TIC(t1_);
-                    bool te = true;
-                    if constexpr (!C::kMergeT) te = mbar_wait(&tempty[buf], ((slab >> 1) & 1) ^ 1, abort_flag);
                     FP8BS_TOC(w_tempty, t1_);
                     FP8BS_TIC(t2_);
-                    const bool fu = te && mbar_wait(&full[st], (iter / S) & 1, abort_flag);
+                    // (the stage's barrier also carries the release of TMEM buffer `buf`)
+                    const bool fu = mbar_wait(&full[st], (iter / S) & 1, abort_flag);
                     FP8BS_TOC(w_full, t2_);
-                    if (!te || !fu) {
+                    if (!fu) {
                         set_abort(abort_flag);
                         ok = false;
                         break;
@@ -778,14 +783,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             const volatile int never = 0;
             if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
         }
-    } else if (C::kFused) {
-        // ---------------------------------------------------------- quantiser
-        // warps 2-3 (and 8-9): act_quant of the token rows of each slab,
-        // written as the e4m3 Q tile in the 128-byte-swizzled layout the MMA reads
-        if constexpr (C::kFused) quantiser_role<BN, S>(p, it, s_prefix, sQ, sX, s_ring, full, xfull, abort_flag);
     }
-    } else if (C::kFused && warp >= kEpiWarp0 + C::kEpiWarps) {
-        if constexpr (C::kFused) quantiser_role<BN, S>(p, it, s_prefix, sQ, sX, s_ring, full, xfull, abort_flag);
     } else {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
         // ---------------------------------------------------------- epilogue
@@ -795,7 +793,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
         const int e = q * 32 + lane;                // row of the tile (TMEM lane)
         const int cofs = ((warp - kEpiWarp0) >> 2) * CPT;   // first tile column of this thread
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t slab = 0, epi_phase = 0, chunk_ctr = 0;
+        uint32_t slab = 0, epi_phase = 0;
         bool ok = true;
         // one finished slab: wait for it in TMEM, promote it, free the buffer
 #ifdef FP8BS_TRACE_ENABLED
@@ -815,17 +813,11 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             tc_fence_after();
             if (slab == 0 && e == 0) FP8BS_TRACE(4);
             FP8BS_TIC(t4_);
-            promote<CPT, is_swap<V>()>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs),
-                                          acc, sc_col, sc);
+            promote<CPT, false>(tmem_base + lane_off + static_cast<uint32_t>(buf * BN + cofs), acc, sc_col, sc);
             FP8BS_TOC(w_promote, t4_);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                if constexpr (C::kMergeT)
-                    mbar_arrive(&full[(slab + 2) % S]);   // the buffer slab + 2 writes is free
-                else
-                    mbar_arrive(&tempty[buf]);
-            }
+            if (lane == 0) mbar_arrive(&full[(slab + 2) % S]);   // the buffer slab + 2 writes is free
             ++slab;
             if (!warp_all(got)) {
                 set_abort(abort_flag);
@@ -838,48 +830,10 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             float acc[CPT];
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
-            if constexpr (V == kSwapFused) {
-                // scale products b_s[block] * a_s[token] come from the quantiser
-                for (int kb = sg.k0; kb < sg.k1 && ok; ++kb)
-                    ok = take_slab(acc, s_ring + (slab % C::kRingSlots) * BN, 0.0f);
-            } else if constexpr (V == kDenseSwap) {
-                // scale products b_s[block] * a_s[token] of 32 slabs at a time,
-                // staged in shared memory one chunk ahead
-                constexpr int CH = kScaleChunk, PER = CH * BN / 128;
-                const float* ps = p.b_s + static_cast<int64_t>(tg.p_row0 / 128) * p.KB;
-                const float* qs = p.a_s + static_cast<int64_t>(tg.q_row0) * p.KB;
-                float pre[PER];
-                auto issue = [&](int base) {
-#pragma unroll
-                    for (int r = 0; r < PER; ++r) {
-                        const int idx = e + r * 128, i = idx / BN, j = idx % BN, kb = base + i;
-                        pre[r] = (kb < sg.k1 && j < tg.q_valid)
-                                     ? __ldg(ps + kb) * __ldg(qs + static_cast<int64_t>(j) * p.KB + kb)
-                                     : 0.0f;
-                    }
-                };
-                auto commit = [&]() {
-                    float* dst = s_scale + (chunk_ctr & 1) * (CH * BN);
-#pragma unroll
-                    for (int r = 0; r < PER; ++r) dst[e + r * 128] = pre[r];
-                };
-                const int n = sg.k1 - sg.k0;
-                issue(sg.k0);
-                for (int rel = 0; rel < n && ok; ++rel) {
-                    const int i = rel % CH;
-                    if (i == 0) {
-                        if (rel > 0) ++chunk_ctr;
-                        commit();
-                        ok = epi_sync(epi_bar, epi_phase, abort_flag);
-                        if (!ok) break;
-                        if (rel + CH < n) issue(sg.k0 + rel + CH);
-                    }
-                    ok = take_slab(acc, s_scale + (chunk_ctr & 1) * (CH * BN) + i * BN, 0.0f);
-                }
-                ++chunk_ctr;
-            } else {
+            {
                 // per-row a_s and per-block b_s, prefetched PF slabs ahead in registers
-                const float* ps = p.a_s + static_cast<int64_t>(e < tg.p_valid ? tg.p_row0 + e : 0) * p.KB;
+                const int arow = e < tg.p_valid ? tg.p_row0 + e : tg.p_row0;
+                const float* ps = p.a_s + static_cast<int64_t>(p.row_token ? __ldg(p.row_token + arow) : arow) * p.KB;
                 // (columns past N read the last block's scales; they are never stored)
                 const float* qs = (V == kDense)
                                       ? p.b_s + static_cast<int64_t>(min((tg.q_row0 + cofs) / 128, p.NB - 1)) * p.KB
@@ -924,6 +878,18 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
                 FP8BS_TIC(t5_);
+                if constexpr (BN == 256) {
+                    if (p.swiglu) {
+                        const int half = (warp - kEpiWarp0) >> 2;
+                        uint8_t* my_box = sStg + (warp - kEpiWarp0) * (C::kStgRows * 128);
+                        const uint8_t* peer_box = sStg + ((warp - kEpiWarp0) ^ 4) * (C::kStgRows * 128);
+                        const int iblk = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) / 256;
+                        swiglu_quant_epilogue<C::kStgRows>(p, my_box, peer_box, half, lane, q, e < tg.p_valid,
+                                                           static_cast<int64_t>(tg.p_row0) + e, iblk, acc);
+                        FP8BS_TOC(w_store, t5_);
+                        continue;
+                    }
+                }
                 if constexpr (C::kTmaStore) {
                     if (p.tma_store) {
                         const int col0 = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) + cofs;
@@ -940,64 +906,9 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                 FP8BS_TOC(w_store, t5_);
                 continue;
             }
-            if constexpr (is_swap<V>()) {
-                if (p.ksplit > 1) {
-                    // ---- cluster split-K: every CTA pushes each tile row of its
-                    // partial to the CTA that owns that row (rank = row / rows)
-                    // with asynchronous remote stores that count as transaction
-                    // bytes on the owner's barrier; the owner, expecting
-                    // 128 x BN x 4 bytes, reduces the c partials in rank order
-                    const int c = p.ksplit, rows = 128 / c;
-                    const uint32_t rank = cluster_rank();
-                    {
-                        const uint32_t owner = static_cast<uint32_t>(e / rows);
-                        const uint32_t dst = cluster_map(
-                            smem_u32(s_recv + (static_cast<int>(rank) * rows + e % rows) * BN), owner);
-                        const uint32_t bar = cluster_map(smem_u32(red_bar), owner);
-#pragma unroll
-                        for (int j = 0; j < BN; j += 4)
-                            st_async_f4(dst + j * 4, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]), bar);
-                    }
-                    if (e == 0) mbar_arrive_expect_tx(red_bar, 128u * BN * 4u);
-                    if (!warp_all(mbar_wait(red_bar, 0, abort_flag))) {
-                        set_abort(abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    if (e == 0) FP8BS_TRACE(10);
-                    // reduce rows [rank*rows, (rank+1)*rows): s_recv[src][row][BN];
-                    // consecutive threads take consecutive rows (= output columns)
-                    const int groups = BN / 4;
-                    for (int idx = e; idx < rows * groups; idx += 128) {
-                        const int lr = idx % rows, g4 = idx / rows;
-                        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int r = 0; r < c; ++r) {
-                            const float4 v = *reinterpret_cast<const float4*>(s_recv + (r * rows + lr) * BN + g4 * 4);
-                            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-                        }
-                        const int row = static_cast<int>(rank) * rows + lr;
-                        const int n = tg.p_row0 + row;
-                        if (row < tg.p_valid) {
-                            const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int j = g4 * 4 + i;
-                                if (j < tg.q_valid) {
-                                    const int64_t o = static_cast<int64_t>(tg.q_row0 + j) * p.N + n;
-                                    if (p.c_bf16) p.c_bf16[o] = __float2bfloat16_rn(vals[i]);
-                                    if (p.c_fp32) p.c_fp32[o] = vals[i];
-                                }
-                            }
-                        }
-                    }
-                    if (e == 0) FP8BS_TRACE(9);
-                    continue;
-                }
-            }
             // ---- stream-K fixup: partial tile.  The 128x256 kernels only
-            // ever run whole tiles and the fused kernel only cluster split-K
-            // (the host plans them so); compiled out of both.
-            if constexpr (C::kSplitRegs || C::kFused) {   // never planned for these
+            // ever run whole tiles (the host plans them so); compiled out there.
+            if constexpr (C::kSplitRegs) {   // never planned for these
                 set_abort(abort_flag);
                 ok = false;
                 break;
@@ -1672,7 +1583,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (warp == 1) tmem_dealloc_pair(tmem_base, 512);
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------ host side
+// Tensor-map helpers, shared with the decode kernels (decode.cu).
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -1716,10 +1630,15 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
     return r == CUDA_SUCCESS;
 }
 
+namespace {
+
 bool wide_tiles_ok();
 
+// Schedule of the dense kernel (M > 64; smaller batches run on the decode
+// kernel): 128x256 tiles per persistent CTA when there are plenty of them,
+// else 128x128 tiles, as whole tiles or as a stream-K split of (tile, slab)
+// units when there are few.
 struct Plan {
-    int variant;   // kDense / kDenseSwap
     int bn;
     int tiles_p, tiles_q, num_tiles;
     int stream_k;
@@ -1727,52 +1646,25 @@ struct Plan {
     long long total_units;
     size_t ws_bytes;   // counters + partial slots
     size_t counters_bytes;
-    int ksplit;        // swapped layout: CTAs (one cluster) per output tile, 0 = not used
 };
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
     Plan pl{};
     const int KB = static_cast<int>(K / kBlock);
-    if (M <= 64) {
-        pl.variant = kDenseSwap;
-        pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-        pl.tiles_p = static_cast<int>((N + 127) / 128);
-        pl.tiles_q = static_cast<int>((M + pl.bn - 1) / pl.bn);
-    } else {
-        pl.variant = kDense;
-        pl.bn = 128;
-        pl.tiles_p = static_cast<int>((M + 127) / 128);
-        pl.tiles_q = static_cast<int>((N + 127) / 128);
-        // enough 128x256 tiles for whole-tile scheduling: use the wide tile
-        const long long wide = static_cast<long long>(pl.tiles_p) * ((N + 255) / 256);
-        if (wide >= 4LL * sms && wide <= (1LL << 30) && KB > 1 && wide_tiles_ok()) {
-            pl.bn = 256;
-            pl.tiles_q = static_cast<int>((N + 255) / 256);
-        }
+    pl.bn = 128;
+    pl.tiles_p = static_cast<int>((M + 127) / 128);
+    pl.tiles_q = static_cast<int>((N + 127) / 128);
+    // enough 128x256 tiles for whole-tile scheduling: use the wide tile
+    const long long wide = static_cast<long long>(pl.tiles_p) * ((N + 255) / 256);
+    if (wide >= 4LL * sms && wide <= (1LL << 30) && KB > 1 && wide_tiles_ok()) {
+        pl.bn = 256;
+        pl.tiles_q = static_cast<int>((N + 255) / 256);
     }
     pl.num_tiles = pl.tiles_p * pl.tiles_q;
     pl.total_units = static_cast<long long>(pl.num_tiles) * KB;
-    const long long slots = static_cast<long long>(sms) * (pl.bn <= 32 ? 2 : 1);
-    if (pl.variant == kDenseSwap && pl.num_tiles <= slots) {
-        // decode: every output tile gets a cluster of c CTAs splitting K (at
-        // least 4 slabs each); c is the largest of 1, 2, 4, 8 that keeps all
-        // CTAs resident at once (two per SM for the small tiles).  With more
-        // tiles than resident CTAs, stream-K below balances the work instead.
-        int c = 1;
-        while (c < 8 && static_cast<long long>(pl.num_tiles) * c * 2 <= slots && KB / (c * 2) >= 4) c *= 2;
-        pl.ksplit = c;
+    if (pl.num_tiles >= 4 * sms || pl.num_tiles > kMaxSkTiles || KB == 1) {
         pl.stream_k = 0;
-        pl.grid = pl.num_tiles * c;
-        pl.ws_bytes = 0;
-        return pl;
-    }
-    // whole tiles per persistent CTA when there are plenty of tiles, and for
-    // the swapped layout whenever its tiles outnumber the resident CTAs (its
-    // stream-K split spreads a tile over many CTAs and the fix-up dominates:
-    // wq_b at M=64 took 28.8 us split, 18.3 us whole)
-    if (pl.num_tiles >= 4 * sms || pl.num_tiles > kMaxSkTiles || KB == 1 || pl.variant == kDenseSwap) {
-        pl.stream_k = 0;
-        pl.grid = static_cast<int>(std::min<long long>(pl.num_tiles, pl.variant == kDenseSwap ? slots : sms));
+        pl.grid = static_cast<int>(std::min<long long>(pl.num_tiles, sms));
         pl.ws_bytes = 0;
     } else {
         pl.stream_k = 1;
@@ -1789,7 +1681,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
 
 template <int BN, int V>
 cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorMap& mc, const Params& prm,
-                   int grid, cudaStream_t st, unsigned cluster = 1) {
+                   int grid, cudaStream_t st) {
     using C = Cfg<BN, V>;
     constexpr int smem = C::kSmemBytes;
     static int configured[64] = {0};
@@ -1801,8 +1693,7 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorM
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    return launch_pdl_cluster(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, cluster, mp, mq, mc,
-                              prm);
+    return launch_pdl(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, mp, mq, mc, prm);
 }
 
 // The 128x256 kernels move registers between warpgroups with setmaxnreg;
@@ -1856,18 +1747,28 @@ extern "C" int fp8_debug_read_trace(unsigned long long* host) {
 }
 #endif
 
+namespace fp8bs {
+// decode.cu: the M <= 64 path of fp8_gemm (xq, a_s) and fp8_linear (x)
+fp8_status decode_gemm(const void* x, const void* xq, const float* a_s, const void* w, const float* b_s,
+                       void* c_bf16, float* c_fp32, int64_t M, int64_t N, int64_t K, int ue8m0, int debug_skip,
+                       cudaStream_t st);
+bool decode_set_wait_limit(long long cycles);
+}  // namespace fp8bs
+
 // Test hooks of the failure path (see fp8_debug_skip_one_arrive).
 static std::atomic<int> g_debug_skip_next{0};
 
 extern "C" fp8_status fp8_debug_set_wait_limit(long long cycles) {
     const long long v = cycles > 0 ? cycles : kWaitLimitCycles;
-    return cudaMemcpyToSymbol(g_wait_limit_cycles, &v, sizeof(v)) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_wait_limit_cycles, &v, sizeof(v)) != cudaSuccess) return FP8_ERR_CUDA;
+    return decode_set_wait_limit(v) ? FP8_OK : FP8_ERR_CUDA;
 }
 
 extern "C" void fp8_debug_skip_one_arrive(void) { g_debug_skip_next.store(1); }
 
 extern "C" size_t fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || K % kBlock != 0) return 0;
+    if (M <= kDecodeMaxM) return 0;   // the decode kernel reduces on chip
     return make_plan(M, N, K, device_sm_count()).ws_bytes;
 }
 
@@ -1896,6 +1797,9 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
                                void* workspace, size_t workspace_bytes, void* stream) {
     const fp8_status chk = gemm_check_args(a, a_s, b, b_s, c_bf16, c_fp32, M, N, K);
     if (chk != FP8_OK || M == 0 || N == 0) return chk;
+    if (M <= kDecodeMaxM)
+        return decode_gemm(nullptr, a, a_s, b, b_s, c_bf16, c_fp32, M, N, K, 0, g_debug_skip_next.exchange(0),
+                           static_cast<cudaStream_t>(stream));
     const Plan pl = make_plan(M, N, K, device_sm_count());
     if (pl.ws_bytes > 0 && (workspace == nullptr || workspace_bytes < pl.ws_bytes))
         return FP8_ERR_WORKSPACE;
@@ -1915,7 +1819,6 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     prm.num_tiles = pl.num_tiles;
     prm.stream_k = pl.stream_k;
     prm.total_units = pl.total_units;
-    prm.ksplit = pl.ksplit;
     prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(b_s)) ? 1 : 0;
     prm.debug_skip = g_debug_skip_next.exchange(0);
 #ifdef FP8BS_TRACE_ENABLED
@@ -1926,27 +1829,15 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
         prm.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes);
     }
     CUtensorMap mp, mq, mc;
-    const bool swap = pl.variant == kDenseSwap;
-    // P: 128-row tiles; Q: BN-row tiles
-    if (!make_map(&mp, swap ? b : a, swap ? N : M, K, 128) ||
-        !make_map(&mq, swap ? a : b, swap ? M : N, K, pl.bn))
-        return FP8_ERR_CUDA;
-    // C (dense, bf16 only, 16-byte rows): 32 x 64 boxes for the TMA tile store
-    prm.tma_store = (!swap && c_bf16 && !c_fp32 && N % 8 == 0) ? 1 : 0;
+    // P: 128-row tiles of the activations; Q: BN-row tiles of the weight
+    if (!make_map(&mp, a, M, K, 128) || !make_map(&mq, b, N, K, pl.bn)) return FP8_ERR_CUDA;
+    // C (bf16 only, 16-byte rows): 32 x 64 boxes for the TMA tile store
+    prm.tma_store = (c_bf16 && !c_fp32 && N % 8 == 0) ? 1 : 0;
     if (prm.tma_store && !make_map_bf16(&mc, c_bf16, M, N, 32)) return FP8_ERR_CUDA;
     if (!prm.tma_store) mc = mp;   // not read
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (!swap) {
-        e = pl.bn == 256 ? launch<256, kDense>(mp, mq, mc, prm, pl.grid, st)
-                         : launch<128, kDense>(mp, mq, mc, prm, pl.grid, st);
-    } else if (pl.bn == 16) {
-        e = launch<16, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
-    } else if (pl.bn == 32) {
-        e = launch<32, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
-    } else {
-        e = launch<64, kDenseSwap>(mp, mq, mc, prm, pl.grid, st, pl.ksplit);
-    }
+    const cudaError_t e = pl.bn == 256 ? launch<256, kDense>(mp, mq, mc, prm, pl.grid, st)
+                                       : launch<128, kDense>(mp, mq, mc, prm, pl.grid, st);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -2051,6 +1942,93 @@ extern "C" fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const vo
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ expert body fused into w1|w3
+namespace {
+fp8_status swiglu_check(int64_t M, int64_t I, int64_t K, int scale_fmt) {
+    if (M < 0 || I <= 0 || K <= 0 || K % kBlock != 0 || I % kBlock != 0) return FP8_ERR_INVALID_ARG;
+    if (scale_fmt != FP8_SCALE_FP32 && scale_fmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+    if (M > (1LL << 31) - 1 || 2 * I > (1LL << 31) - 1 || K > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    return FP8_OK;
+}
+}  // namespace
+
+extern "C" fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const void* w13, const float* w13_s,
+                                      void* g_q, float* g_s, int64_t M, int64_t I, int64_t K, int scale_fmt,
+                                      void* stream) {
+    const fp8_status chk = swiglu_check(M, I, K, scale_fmt);
+    if (chk != FP8_OK || M == 0) return chk;
+    if (!a || !a_s || !w13 || !w13_s || !g_q || !g_s || !aligned16(a) || !aligned16(w13) || !aligned16(g_q))
+        return FP8_ERR_INVALID_ARG;
+    if (!wide_tiles_ok()) return FP8_ERR_UNSUPPORTED;
+    Params prm{};
+    prm.a_s = a_s;
+    prm.b_s = w13_s;
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(2 * I);
+    prm.KB = static_cast<int>(K / kBlock);
+    prm.NB = static_cast<int>(2 * I / 128);
+    prm.G = 1;
+    prm.tiles_p = static_cast<int>((M + 127) / 128);
+    prm.tiles_q = static_cast<int>(I / 128);   // one 128 x 256 tile per 128-wide block of I
+    const int64_t tiles = static_cast<int64_t>(prm.tiles_p) * prm.tiles_q;
+    if (tiles > (1LL << 30)) return FP8_ERR_UNSUPPORTED;
+    prm.num_tiles = static_cast<int>(tiles);
+    prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(w13_s)) ? 1 : 0;
+    prm.swiglu = 1;
+    prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
+    prm.gq = static_cast<uint8_t*>(g_q);
+    prm.gs = g_s;
+#ifdef FP8BS_TRACE_ENABLED
+    prm.trace_slot = g_trace_next++ & 3;
+#endif
+    CUtensorMap mp, mq;
+    if (!make_map(&mp, a, M, K, 128) || !make_map(&mq, w13, 2 * I, K, 256)) return FP8_ERR_CUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, device_sm_count()));
+    const cudaError_t e = launch<256, kDense>(mp, mq, mp, prm, grid, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" fp8_status fp8_moe_expert_up(const void* xq, const float* xs, int64_t T, const int32_t* row_token,
+                                        const void* w13, const float* w13_s, const int32_t* offsets, int32_t G,
+                                        int64_t R_max, void* g_q, float* g_s, int64_t I, int64_t K, int scale_fmt,
+                                        void* stream) {
+    const fp8_status chk = swiglu_check(R_max, I, K, scale_fmt);
+    if (chk != FP8_OK) return chk;
+    if (G < 0 || G > kMaxGroups || T < 0) return FP8_ERR_INVALID_ARG;
+    if (G == 0 || R_max == 0 || T == 0) return FP8_OK;
+    if (static_cast<int64_t>(G) * 2 * I > (1LL << 31) - 1 || T > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    if (!xq || !xs || !row_token || !w13 || !w13_s || !offsets || !g_q || !g_s || !aligned16(xq) ||
+        !aligned16(w13) || !aligned16(g_q))
+        return FP8_ERR_INVALID_ARG;
+    if (!wide_tiles_ok()) return FP8_ERR_UNSUPPORTED;
+    Params prm{};
+    prm.a_s = xs;
+    prm.b_s = w13_s;
+    prm.offsets = offsets;
+    prm.M = static_cast<int>(R_max);
+    prm.N = static_cast<int>(2 * I);
+    prm.KB = static_cast<int>(K / kBlock);
+    prm.NB = static_cast<int>(2 * I / 128);
+    prm.G = G;
+    prm.stream_k = 0;
+    prm.vec_scales = (prm.KB % 4 == 0 && aligned16(xs) && aligned16(w13_s)) ? 1 : 0;
+    prm.swiglu = 1;
+    prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
+    prm.gq = static_cast<uint8_t*>(g_q);
+    prm.gs = g_s;
+    prm.row_token = row_token;
+#ifdef FP8BS_TRACE_ENABLED
+    prm.trace_slot = g_trace_next++ & 3;
+#endif
+    CUtensorMap mp, mq;
+    // A: token rows gathered four at a time (box one row high); B: the experts' w1|w3
+    if (!make_map(&mp, xq, T, K, 1) || !make_map(&mq, w13, static_cast<int64_t>(G) * 2 * I, K, 256))
+        return FP8_ERR_CUDA;
+    const cudaError_t e =
+        launch<256, kGrouped>(mp, mq, mp, prm, device_sm_count(), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ no-allocation variant
 // Some callers cannot allocate device memory at the point where they run a
 // linear layer: code that must not call cudaMalloc (which can synchronise the
@@ -2111,20 +2089,11 @@ extern "C" fp8_status fp8_gemm_noalloc(const void* a, const float* a_s, const vo
 namespace {
 constexpr size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// The fused kernel saves the act_quant launch and its dependency hop, but
-// every CTA quantises its own slabs (redundantly across output tiles) on
-// four warps, which must keep pace with the weight stream.  Measured at M=16
-// on GB300, whole decode step (wq_a, wq_b, wo): 50.0 us with only wq_a (7
-// slabs per CTA) fused, 49.3 us with all three (wo: 32 slabs per CTA)
-// fused; longer K ranges per CTA are not measured and stay staged.
-constexpr int kFusedMaxSlabsPerCta = 64;
-
-bool linear_is_fused(int64_t M, int64_t N, int64_t K) {
-    if (M > 16) return false;
-    const Plan pl = make_plan(M, N, K, device_sm_count());
-    return pl.variant == kDenseSwap && pl.ksplit > 0 && pl.bn == 16 &&
-           (K / kBlock + pl.ksplit - 1) / pl.ksplit <= kFusedMaxSlabsPerCta;
-}
+// Batches up to 16 tokens quantise the activations inside the decode kernel
+// (each CTA quantises its own K range; a 16-token slab is 2 KB of codes);
+// larger batches stage act_quant's codes and scales in the workspace and
+// run fp8_gemm on them.
+bool linear_is_fused(int64_t M, int64_t, int64_t) { return M <= kDecodeFusedMaxM; }
 
 // Staged fp8_linear workspace: [fp8_gemm's region][codes][scales].  The
 // region in front is never shorter than the split-tile counters, which must
@@ -2169,28 +2138,8 @@ extern "C" fp8_status fp8_linear(const void* x, const void* w, const float* w_s,
     }
     if ((c_bf16 && (reinterpret_cast<uintptr_t>(c_bf16) & 1)) || (c_fp32 && (reinterpret_cast<uintptr_t>(c_fp32) & 3)))
         return FP8_ERR_INVALID_ARG;
-    const Plan pl = make_plan(M, N, K, device_sm_count());
-    Params prm{};
-    prm.b_s = w_s;
-    prm.c_bf16 = static_cast<__nv_bfloat16*>(c_bf16);
-    prm.c_fp32 = c_fp32;
-    prm.M = static_cast<int>(M);
-    prm.N = static_cast<int>(N);
-    prm.KB = static_cast<int>(K / kBlock);
-    prm.NB = static_cast<int>((N + 127) / 128);
-    prm.G = 1;
-    prm.tiles_p = pl.tiles_p;
-    prm.tiles_q = pl.tiles_q;
-    prm.num_tiles = pl.num_tiles;
-    prm.ksplit = pl.ksplit;
-    prm.x = static_cast<const uint16_t*>(x);
-    prm.K = K;
-    prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
-#ifdef FP8BS_TRACE_ENABLED
-    prm.trace_slot = g_trace_next++ & 3;
-#endif
-    CUtensorMap mp, mx;
-    if (!make_map(&mp, w, N, K, 128) || !make_map_bf16(&mx, x, M, K, 16)) return FP8_ERR_CUDA;
-    const cudaError_t e = launch<16, kSwapFused>(mp, mx, mp, prm, pl.grid, st, pl.ksplit);
-    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+    // decode batches: the quantisation runs inside the decode kernel, whose
+    // plan is fp8_gemm's for the same shape (bit-identical results)
+    return decode_gemm(x, nullptr, nullptr, w, w_s, c_bf16, c_fp32, M, N, K, scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0, 0,
+                       st);
 }

@@ -202,14 +202,9 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; i += 2) {
-                const float s0 = a[i] / (1.0f + expf(-a[i]));
-                const float s1 = a[i + 1] / (1.0f + expf(-a[i + 1]));
-                const float sb0 = __bfloat162float(__float2bfloat16_rn(s0));
-                const float sb1 = __bfloat162float(__float2bfloat16_rn(s1));
-                const __nv_bfloat162 gb = __floats2bfloat162_rn(sb0 * b[i], sb1 * b[i + 1]);
-                gbits[i / 2] = *reinterpret_cast<const uint32_t*>(&gb);
-                gv[i] = __low2float(gb);
-                gv[i + 1] = __high2float(gb);
+                gbits[i / 2] = silu_mul_bf16x2(a[i], a[i + 1], b[i], b[i + 1]);
+                gv[i] = __uint_as_float(gbits[i / 2] << 16);
+                gv[i + 1] = __uint_as_float(gbits[i / 2] & 0xFFFF0000u);
                 amax = fmaxf(amax, fmaxf(fabsf(gv[i]), fabsf(gv[i + 1])));
             }
             amax = half_warp_max(amax);

@@ -176,6 +176,40 @@ fp8_status fp8_grouped_gemm(const void* a, const float* a_s, const void* b, cons
                             const int32_t* offsets, int32_t G, int64_t R_max,
                             void* c_bf16, float* c_fp32, int64_t N, int64_t K, void* stream);
 
+/* The first half of the MLP / expert body with its gate fused in
+ * (behavior-traces page, "MoE trace": each expert computes
+ * w2(silu(w1 x) * w3 x); source tour, "FP8 with per-block scales": every
+ * linear's input is quantised per 128 block): the block-scaled products
+ * h1 = a w1^T and h3 = a w3^T, then g = bf16(bf16(silu(h1)) * h3) with h1, h3
+ * rounded to bf16, then act_quant(g) -> g_q [M, I] e4m3 and g_s [M, I/128]
+ * fp32 -- the same bytes as fp8_gemm (bf16 out) followed by
+ * fp8_silu_mul_quant, without h ever leaving the chip.
+ * w13 [2I, K] e4m3 holds w1 and w3 INTERLEAVED by 128-row blocks: rows
+ * [256 j, 256 j + 128) are w1's rows [128 j, 128 j + 128) and rows
+ * [256 j + 128, 256 j + 256) are w3's same rows; w13_s [2I/128, K/128]
+ * follows the same block order.  a [M, K] e4m3 with a_s [M, K/128].
+ * Requires I % 128 == 0, K % 128 == 0, 16-byte aligned a, w13, g_q.
+ * scale_fmt is g's scale format.  No workspace.  M == 0 is a no-op. */
+fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const void* w13, const float* w13_s, void* g_q,
+                           float* g_s, int64_t M, int64_t I, int64_t K, int scale_fmt, void* stream);
+
+/* The routed experts' first half in one launch (behavior-traces page, "MoE
+ * trace": tokens gathered per expert, then w2(silu(w1 x) * w3 x); source
+ * tour, "Honest Limits": a fused grouped GEMM instead of the per-expert
+ * loop).  Packed row r (expert g owns rows [offsets[g], offsets[g+1])) is
+ * token row_token[r] of xq [T, K] e4m3 (scales xs [T, K/128]), gathered by
+ * the GEMM's loads (no packed copy of the activations); each expert's w13
+ * ([G, 2I, K], interleaved as for fp8_gemm_swiglu; scales [G, 2I/128,
+ * K/128]) makes h1, h3, and the gate and act_quant run in the epilogue ->
+ * g_q [R_max, I] e4m3, g_s [R_max, I/128] in packed row order (rows past
+ * offsets[G] are not written).  offsets and row_token: int32, device.  The
+ * same bytes as fp8_moe_gather + fp8_grouped_gemm + fp8_silu_mul_quant.
+ * Requires I % 128 == 0, K % 128 == 0, 16-byte aligned xq, w13, g_q. */
+fp8_status fp8_moe_expert_up(const void* xq, const float* xs, int64_t T, const int32_t* row_token,
+                             const void* w13, const float* w13_s, const int32_t* offsets, int32_t G,
+                             int64_t R_max, void* g_q, float* g_s, int64_t I, int64_t K, int scale_fmt,
+                             void* stream);
+
 /* Expert body between the two grouped GEMMs, fused with act_quant: for
  * rows r < R and columns i < I,
  *   g = bf16(bf16(silu(h1)) * h3),  silu(v) = v / (1 + exp(-v)) in fp32,

@@ -63,9 +63,11 @@ def test_gemm_reads_fresh_weights(fp8, M):
     _chained_vs_settled(fp8, lambda q, s: fp8.fp8_gemm(xq, xs, q, s)[0], N, K)
 
 
-def test_gemm_reads_activations_quantised_just_before(fp8):
-    # act_quant writes the codes and scales fp8_gemm reads next, round after round
-    M, N, K = 256, 1024, 2048
+@pytest.mark.parametrize("M", [16, 64, 256])
+def test_gemm_reads_activations_quantised_just_before(fp8, M):
+    # act_quant writes the codes and scales fp8_gemm reads next, round after
+    # round (the decode kernel at M = 16 and 64, the dense one at M = 256)
+    N, K = 1024, 2048
     w, w_s = fp8.fp8_weight_quant(syn.normal_bf16_device((N, K), 0.02, 520, "cuda"))
     xq = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
     xs = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
@@ -80,6 +82,28 @@ def test_gemm_reads_activations_quantised_just_before(fp8):
         q, s = fp8.fp8_act_quant(x)
         torch.cuda.synchronize()
         settled = fp8.fp8_gemm(q, s, w, w_s)[0]
+        torch.cuda.synchronize()
+        assert torch.equal(chained[i].view(torch.int16), settled.view(torch.int16)), f"round {i}: stale inputs read"
+    fp8.fp8_device_status()
+
+
+def test_linear_reads_activations_written_just_before(fp8):
+    # weight_dequant writes the bf16 activations the fused decode linear
+    # quantises next, round after round
+    M, N, K = 16, 1536, 7168
+    w, w_s = fp8.fp8_weight_quant(syn.normal_bf16_device((N, K), 0.02, 530, "cuda"))
+    src = [fp8.fp8_weight_quant(syn.normal_bf16_device((M, K), 1.0, 531 + i, "cuda")) for i in range(4)]
+    x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    chained = []
+    for q, s in src:
+        fp8.fp8_weight_dequant(q, s, y=x)
+        chained.append(fp8.fp8_linear(x, w, w_s)[0].clone())
+    torch.cuda.synchronize()
+    for i, (q, s) in enumerate(src):
+        xi = fp8.fp8_weight_dequant(q, s)
+        torch.cuda.synchronize()
+        settled = fp8.fp8_linear(xi, w, w_s)[0]
         torch.cuda.synchronize()
         assert torch.equal(chained[i].view(torch.int16), settled.view(torch.int16)), f"round {i}: stale inputs read"
     fp8.fp8_device_status()

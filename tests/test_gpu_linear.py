@@ -1,8 +1,9 @@
 """GPU parity of fp8_linear, the model's FP8 linear in one call (source
 tour, "FP8 with per-block scales": act_quant of the activations, then
-fp8_gemm).  For small decode batches the quantisation runs inside the GEMM
-kernel; the result must equal act_quant followed by fp8_gemm bit for bit
-and match the oracle's exact block-scaled product."""
+fp8_gemm).  For decode batches of up to 16 tokens the quantisation runs
+inside the decode GEMM kernel; larger batches stage act_quant's codes in the
+workspace.  Either way the result must equal act_quant followed by fp8_gemm
+bit for bit and match the oracle's exact block-scaled product."""
 import numpy as np
 import pytest
 import torch
@@ -41,18 +42,36 @@ def _compare(fp8, x_bits, w_bits, ue8m0, what, expect_fused=None):
     check_gemm(ref, mag, host_f32(lf), host_bits(lb), what)
 
 
-@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 48, 64])
 def test_decode_linears(fp8, M):
-    # every decode layer at M <= 16 runs the fused kernel (7, 12 and 32 slabs
-    # per CTA for wq_a, wq_b and wo)
+    # every decode layer on the decode kernel: 16-token tiles with the
+    # quantisation fused, 32- and 64-token tiles after act_quant; clusters
+    # of up to 16 CTAs splitting K
     for lin in syn.decode_linears(M):
-        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M={M}", expect_fused=True)
+        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M={M}", expect_fused=M <= 16)
 
 
-def test_decode_linears_staged_above_16_tokens(fp8):
-    # M = 33: act_quant into the workspace, then fp8_gemm
-    for lin in syn.decode_linears(33):
-        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M=33", expect_fused=False)
+def test_staged_above_64_tokens(fp8):
+    # M = 65: act_quant into the workspace, then fp8_gemm
+    for lin in syn.decode_linears(65, layers=["wq_a", "wo"]):
+        _compare(fp8, lin.x, lin.w, False, f"{lin.name} M=65", expect_fused=False)
+
+
+@pytest.mark.parametrize("shape", [(16, 128, 2048), (40, 128, 2048), (64, 40960, 256), (1, 640, 16384)])
+def test_decode_cluster_and_wave_shapes(fp8, shape):
+    # one tile split 16 ways (the largest cluster); 320 tiles, more than the
+    # CTAs that fit at once (whole tiles in waves); a long K range at M = 1
+    M, N, K = shape
+    rng = np.random.default_rng(N + M)
+    x = syn.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = syn.to_bf16_bits(0.02 * rng.standard_normal((N, K)).astype(np.float32))
+    _compare(fp8, x, w, False, f"{M}x{N}x{K}", expect_fused=M <= 16)
+
+
+@pytest.mark.parametrize("M", [23, 61])
+def test_ue8m0_ragged_wider_batches(fp8, M):
+    lin = syn.ragged_ue8m0(M)
+    _compare(fp8, lin.x, lin.w, True, f"wkv_a M={M} ue8m0", expect_fused=False)
 
 
 def test_fused_ue8m0_ragged_n(fp8):
@@ -69,7 +88,8 @@ def test_fused_short_k_ranges(fp8, K):
 
 
 @pytest.mark.parametrize("M", [37, 2049])
-def test_staged_ragged_ue8m0(fp8, M):
+def test_ragged_ue8m0(fp8, M):
+    # staged: M = 37 on the decode kernel (64-token tile), M = 2049 on the dense one
     lin = syn.ragged_ue8m0(M)
     _compare(fp8, lin.x, lin.w, True, f"wkv_a M={M} ue8m0", expect_fused=False)
 
@@ -93,10 +113,9 @@ def test_fused_special_blocks(fp8):
 
 
 def test_staged_workspace_keeps_counters_clear(fp8):
-    # one workspace, staged calls in a row: wq_a's GEMM needs no workspace of
-    # its own, wq_b's (M=33) splits tiles through the workspace counters, which
-    # the first call's staged codes must not have touched
-    M = 33
+    # one workspace, staged calls in a row (M = 65): both GEMMs split tiles
+    # through the workspace counters, which the staged codes must not touch
+    M = 65
     lins = syn.decode_linears(M, layers=["wq_a", "wq_b"])
     need = max(int(fp8.lib.fp8_linear_workspace_size(M, l.w.shape[0], l.w.shape[1])) for l in lins)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
