@@ -54,8 +54,8 @@ def _declare(lib):
         "fp8_linear": (st, [vp, vp, f32p, vp, f32p, i64, i64, i64, ctypes.c_int, vp, sz, vp]),
         "fp8_gemm_noalloc": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, vp]),
         "fp8_gemm_swiglu": (st, [vp, f32p, vp, f32p, vp, f32p, i64, i64, i64, ctypes.c_int, vp]),
-        "fp8_moe_expert_up": (st, [vp, f32p, i64, vp, vp, f32p, vp, i32, i64, vp, f32p, i64, i64, ctypes.c_int,
-                                   vp]),
+        "fp8_moe_expert_up": (st, [vp, f32p, vp, f32p, vp, i32, i64, vp, f32p, i64, i64, ctypes.c_int, vp]),
+        "fp8_moe_quant_scatter": (st, [vp, vp, i64, i32, i64, vp, f32p, ctypes.c_int, vp]),
         "fp8_debug_set_wait_limit": (st, [ctypes.c_longlong]),
         "fp8_debug_skip_one_arrive": (None, []),
         "fp8_device_status": (st, [vp]),
@@ -319,29 +319,40 @@ def fp8_gemm_swiglu(a, a_s, w13, w13_s, scale_fmt=FP8_SCALE_FP32, g_q=None, g_s=
     return g_q, g_s
 
 
-def fp8_moe_expert_up(xq, xs, row_token, w13, w13_s, offsets, scale_fmt=FP8_SCALE_FP32, g_q=None, g_s=None,
-                      stream=None):
-    """Gather + grouped w1|w3 + silu*mul + act_quant in one launch.  xq [T, K]
-    e4m3 / xs [T, K/128]; row_token int32 [R]; w13 [G, 2I, K] interleaved;
-    offsets int32 [G+1].  Returns (g_q [R, I], g_s [R, I/128])."""
-    _cuda(xq, "xq", _E4M3, 2)
-    _cuda(xs, "xs", _F32, 2)
-    _cuda(row_token, "row_token", _I32, 1)
+def fp8_moe_expert_up(a, a_s, w13, w13_s, offsets, scale_fmt=FP8_SCALE_FP32, g_q=None, g_s=None, stream=None):
+    """Grouped w1|w3 + silu*mul + act_quant in one launch over packed rows.
+    a [R, K] e4m3 / a_s [R, K/128]; w13 [G, 2I, K] interleaved (see
+    interleave_w13); offsets int32 [G+1].  Returns (g_q [R, I], g_s [R, I/128])."""
+    _cuda(a, "a", _E4M3, 2)
+    _cuda(a_s, "a_s", _F32, 2)
     _cuda(w13, "w13", _E4M3, 3)
     _cuda(w13_s, "w13_s", _F32, 3)
     _cuda(offsets, "offsets", _I32, 1)
-    T, K = xq.shape
+    R, K = a.shape
     G, N2, Kw = w13.shape
     I = N2 // 2
-    R = row_token.numel()
     if Kw != K or offsets.numel() != G + 1:
         raise ValueError("shape mismatch")
-    g_q = _empty_e4m3((R, I), xq.device) if g_q is None else g_q
-    g_s = torch.empty((R, I // BLOCK), dtype=torch.float32, device=xq.device) if g_s is None else g_s
-    _check("fp8_moe_expert_up", lib.fp8_moe_expert_up(_ptr(xq), _ptr(xs), T, _ptr(row_token), _ptr(w13), _ptr(w13_s),
-                                                      _ptr(offsets), G, R, _ptr(g_q), _ptr(g_s), I, K,
-                                                      int(scale_fmt), _stream(stream)))
+    g_q = _empty_e4m3((R, I), a.device) if g_q is None else g_q
+    g_s = torch.empty((R, I // BLOCK), dtype=torch.float32, device=a.device) if g_s is None else g_s
+    _check("fp8_moe_expert_up", lib.fp8_moe_expert_up(_ptr(a), _ptr(a_s), _ptr(w13), _ptr(w13_s), _ptr(offsets), G, R,
+                                                      _ptr(g_q), _ptr(g_s), I, K, int(scale_fmt), _stream(stream)))
     return g_q, g_s
+
+
+def fp8_moe_quant_scatter(x, pair_row, scale_fmt=FP8_SCALE_FP32, aq=None, as_=None, stream=None):
+    """act_quant of x [T, K] bf16 written to the packed rows pair_row [T, topk]
+    -> (aq [T*topk, K] e4m3, as [T*topk, K/128] fp32)."""
+    _cuda(x, "x", _BF16, 2)
+    _cuda(pair_row, "pair_row", _I32, 2)
+    T, K = x.shape
+    topk = pair_row.shape[1]
+    R = T * topk
+    aq = _empty_e4m3((R, K), x.device) if aq is None else aq
+    as_ = torch.empty((R, K // BLOCK), dtype=torch.float32, device=x.device) if as_ is None else as_
+    _check("fp8_moe_quant_scatter", lib.fp8_moe_quant_scatter(_ptr(x), _ptr(pair_row), T, topk, K, _ptr(aq),
+                                                              _ptr(as_), int(scale_fmt), _stream(stream)))
+    return aq, as_
 
 
 def fp8_silu_mul_quant(h1, h3, ld_h, R, I, scale_fmt=FP8_SCALE_FP32, want_g=False, y=None, s=None,

@@ -164,13 +164,16 @@ __device__ __forceinline__ void unpack_bf16x8_neg(const uint4& v, float (&nx)[8]
 
 // The expert body's gate for one element pair: g = bf16(bf16(silu(h1)) * h3)
 // with silu(v) = v / (1 + exp(-v)) in fp32, from bf16 inputs given as fp32
-// (exact).  The one routine of the library for it: the standalone
-// silu*mul+act_quant kernel and the GEMM epilogues that fuse it both call
-// it, so their results agree bit for bit.  Returns the two bf16 results
-// packed (first in the low half).
+// (exact).  The exponential and the quotient use the fast hardware
+// approximations (__expf, __fdividef: relative errors of a few fp32 ulps,
+// far below the bf16 rounding that follows; for v < -87 the quotient is
+// +-0, as is the bf16 of the exact value).  The one routine of the library
+// for it: the standalone silu*mul+act_quant kernel and the GEMM epilogue
+// that fuses it both call it, so their results agree bit for bit.  Returns
+// the two bf16 results packed (first in the low half).
 __device__ __forceinline__ uint32_t silu_mul_bf16x2(float a0, float a1, float b0, float b1) {
-    const float s0 = a0 / (1.0f + expf(-a0));
-    const float s1 = a1 / (1.0f + expf(-a1));
+    const float s0 = __fdividef(a0, 1.0f + __expf(-a0));
+    const float s1 = __fdividef(a1, 1.0f + __expf(-a1));
     const float sb0 = __bfloat162float(__float2bfloat16_rn(s0));
     const float sb1 = __bfloat162float(__float2bfloat16_rn(s1));
     const __nv_bfloat162 g = __floats2bfloat162_rn(sb0 * b0, sb1 * b1);
@@ -245,18 +248,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Row gather: four rows (y0..y3) of a 2-D tensor, each one box wide starting
-// at column x, into four consecutive rows of shared memory (the tensor map's
-// box is one row high); completion counted on `bar` as transaction bytes.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* tmap, uint64_t* bar, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
         : "memory");
 }
 

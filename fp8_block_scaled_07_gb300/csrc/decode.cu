@@ -79,8 +79,17 @@ constexpr int kDecMaxCluster = 16;
 #ifndef FP8BS_DEC_S64
 #define FP8BS_DEC_S64 3
 #endif
+// Percent of the device's CTA slots one launch may take.  16-token tiles
+// (three CTAs per SM): half, so the next launch's CTAs are resident and
+// waiting when this one ends (measured on GB300, decode step at M = 16:
+// 40.9 us at half against 50.4 us at all slots); 32- and 64-token tiles (two
+// per SM): all, their streams need the bytes in flight (M = 64: 74.1 us
+// against 85.4 us).
+#ifndef FP8BS_DEC_FILL16
+#define FP8BS_DEC_FILL16 50
+#endif
 #ifndef FP8BS_DEC_FILL
-#define FP8BS_DEC_FILL 50   // percent of the device's CTA slots one launch may take
+#define FP8BS_DEC_FILL 100
 #endif
 
 template <int BN>
@@ -542,7 +551,8 @@ DecPlan decode_plan(int64_t M, int64_t N, int64_t K, int sms, int cmax) {
     pl.tiles = static_cast<int>((N + 127) / 128);
     const int KB = static_cast<int>(K / kBlock);
     const int per_sm = pl.bn == 16 ? Dec<16>::kMinBlocks : (pl.bn == 32 ? Dec<32>::kMinBlocks : Dec<64>::kMinBlocks);
-    const long long budget = std::max<long long>(1, static_cast<long long>(sms) * per_sm * FP8BS_DEC_FILL / 100);
+    const int fill = pl.bn == 16 ? FP8BS_DEC_FILL16 : FP8BS_DEC_FILL;
+    const long long budget = std::max<long long>(1, static_cast<long long>(sms) * per_sm * fill / 100);
     int best_c = 1, best_max = KB;
     for (int c = 2; c <= std::min(cmax, KB); ++c) {
         if (static_cast<long long>(pl.tiles) * c > budget) break;

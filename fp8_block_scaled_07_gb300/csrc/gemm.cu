@@ -115,17 +115,13 @@ struct Params {
     int tma_store;             // dense, bf16 only: full tiles leave through shared memory and TMA
     int vec_scales;            // scale rows are 16-byte aligned (K/128 % 4 == 0, aligned bases)
     int debug_skip;            // test hook: the MMA issuer skips its arrive on slab 0's TMEM-full barrier
-    // expert body fused into the epilogue of the w1|w3 product (128x256 tiles;
-    // weights interleaved so a tile holds h1 and h3 of one 128-wide block):
-    // g = bf16(bf16(silu(h1)) * h3) -> act_quant -> gq [rows, N/2] e4m3,
-    // gs [rows, N/256] fp32, instead of storing h
-    int swiglu;
-    int ue8m0;                 // swiglu: scale format of g's codes
+    // the kernels with the expert body fused into the epilogue of the w1|w3
+    // product (128x256 tiles; weights interleaved so a tile holds h1 and h3
+    // of one 128-wide block): g = bf16(bf16(silu(h1)) * h3) -> act_quant ->
+    // gq [rows, N/2] e4m3, gs [rows, N/256] fp32, instead of storing h
+    int ue8m0;                 // scale format of g's codes
     uint8_t* gq;
     float* gs;
-    // grouped: A rows gathered from the token rows row_token[r] of a [T, K]
-    // matrix (the producer's TMA row gather) instead of read packed
-    const int32_t* row_token;
 };
 
 struct Tile {
@@ -575,7 +571,9 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const v
     return ok;
 }
 
-template <int BN, int V>
+// SW: the expert body fused into the epilogue (a kernel of its own, so
+// that the plain kernels' register allocation does not carry it)
+template <int BN, int V, bool SW>
 __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlocks))
     gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_c, const Params p) {
@@ -681,9 +679,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
     if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        // (gathered A rows: the whole warp, one 4-row TMA gather per lane)
-        const bool gather = (V == kGrouped) && p.row_token != nullptr;
-        if (gather || lane == 0) {
+        if (lane == 0) {
             uint32_t iter = 0;
             bool ok = true;
 #ifdef FP8BS_TRACE_ENABLED
@@ -691,22 +687,11 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
 #endif
             while (ok && it.next(sg)) {
                 const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
-                // token rows of tile rows 4 lane .. 4 lane + 3 (rows past the
-                // expert's last repeat a valid one; their results are not stored)
-                int tok[4] = {0, 0, 0, 0};
-                if (gather) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        tok[i] = __ldg(p.row_token + tg.p_row0 + min(4 * lane + i, tg.p_valid - 1));
-                }
                 for (int kb = sg.k0; kb < sg.k1; ++kb, ++iter) {
                     const int st = iter % S;
                     FP8BS_TIC(t0_);
-                    bool free_st = true;
-                    if (lane == 0) free_st = mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag);
-                    if (gather) free_st = __shfl_sync(0xFFFFFFFFu, free_st ? 1 : 0, 0) != 0;
-                    if (!free_st) {
-                        if (lane == 0) set_abort(abort_flag);
+                    if (!mbar_wait(&empty[st], ((iter / S) & 1) ^ 1, abort_flag)) {
+                        set_abort(abort_flag);
                         ok = false;
                         break;
                     }
@@ -716,26 +701,17 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
                         FP8BS_TRACE(8);
                         FP8BS_TRACE(2);
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&full[st], C::kStageBytes);
-                    if (gather) {
-                        __syncwarp();
-                        tma_gather4(sP + st * kPTileBytes + lane * 4 * 128, &tm_p, &full[st], kb * kBlock, tok[0],
-                                    tok[1], tok[2], tok[3]);
-                        if (lane == 0) tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
-                    } else {
-                        tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
-                        tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
-                    }
+                    mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+                    tma_load_2d(sP + st * kPTileBytes, &tm_p, &full[st], kb * kBlock, tg.p_row0);
+                    tma_load_2d(sQ + st * C::kQTileBytes, &tm_q, &full[st], kb * kBlock, tg.q_row0);
                 }
             }
             FP8BS_TRACE_VAL(11, static_cast<unsigned long long>(w_empty));
             // drain: every load issued must land before the CTA may exit
-            if (lane == 0) {
-                for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
-                    const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
-                    const volatile int never = 0;
-                    if (!mbar_wait(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
-                }
+            for (int st = 0; st < S && st < static_cast<int>(iter); ++st) {
+                const uint32_t uses = iter / S + (static_cast<uint32_t>(st) < iter % S ? 1u : 0u);
+                const volatile int never = 0;
+                if (!mbar_wait(&full[st], (uses - 1) & 1, &never)) set_abort(abort_flag);
             }
         }
     } else if (warp == 1) {
@@ -832,8 +808,7 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
             {
                 // per-row a_s and per-block b_s, prefetched PF slabs ahead in registers
-                const int arow = e < tg.p_valid ? tg.p_row0 + e : tg.p_row0;
-                const float* ps = p.a_s + static_cast<int64_t>(p.row_token ? __ldg(p.row_token + arow) : arow) * p.KB;
+                const float* ps = p.a_s + static_cast<int64_t>(e < tg.p_valid ? tg.p_row0 + e : 0) * p.KB;
                 // (columns past N read the last block's scales; they are never stored)
                 const float* qs = (V == kDense)
                                       ? p.b_s + static_cast<int64_t>(min((tg.q_row0 + cofs) / 128, p.NB - 1)) * p.KB
@@ -878,8 +853,8 @@ __global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlock
             if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
                 FP8BS_TIC(t5_);
-                if constexpr (BN == 256) {
-                    if (p.swiglu) {
+                if constexpr (SW && BN == 256) {
+                    {
                         const int half = (warp - kEpiWarp0) >> 2;
                         uint8_t* my_box = sStg + (warp - kEpiWarp0) * (C::kStgRows * 128);
                         const uint8_t* peer_box = sStg + ((warp - kEpiWarp0) ^ 4) * (C::kStgRows * 128);
@@ -1679,7 +1654,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
     return pl;
 }
 
-template <int BN, int V>
+template <int BN, int V, bool SW = false>
 cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorMap& mc, const Params& prm,
                    int grid, cudaStream_t st) {
     using C = Cfg<BN, V>;
@@ -1688,22 +1663,22 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorM
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, V>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, V, SW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    return launch_pdl(gemm_kernel<BN, V>, dim3(grid), dim3(C::kThreads), smem, st, mp, mq, mc, prm);
+    return launch_pdl(gemm_kernel<BN, V, SW>, dim3(grid), dim3(C::kThreads), smem, st, mp, mq, mc, prm);
 }
 
 // The 128x256 kernels move registers between warpgroups with setmaxnreg;
 // that is only safe if the kernel was built with the register count the
 // split assumes (launch total >= the sum of the new per-warpgroup counts).
-template <int V>
+template <int V, bool SW>
 bool split_regs_ok() {
     using C = Cfg<256, V>;
     cudaFuncAttributes a{};
-    if (cudaFuncGetAttributes(&a, gemm_kernel<256, V>) != cudaSuccess) return false;
+    if (cudaFuncGetAttributes(&a, gemm_kernel<256, V, SW>) != cudaSuccess) return false;
     return a.numRegs * C::kThreads >= C::kRegsLow * 128 + C::kRegsHigh * 32 * C::kEpiWarps;
 }
 
@@ -1711,7 +1686,11 @@ bool wide_tiles_ok() {
     static int cache[64] = {0};   // 0 unknown, 1 yes, 2 no
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return false;
-    if (cache[dev] == 0) cache[dev] = (split_regs_ok<kDense>() && split_regs_ok<kGrouped>()) ? 1 : 2;
+    if (cache[dev] == 0)
+        cache[dev] = (split_regs_ok<kDense, false>() && split_regs_ok<kGrouped, false>() &&
+                      split_regs_ok<kDense, true>() && split_regs_ok<kGrouped, true>())
+                         ? 1
+                         : 2;
     return cache[dev] == 1;
 }
 
@@ -1974,7 +1953,6 @@ extern "C" fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const voi
     if (tiles > (1LL << 30)) return FP8_ERR_UNSUPPORTED;
     prm.num_tiles = static_cast<int>(tiles);
     prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(w13_s)) ? 1 : 0;
-    prm.swiglu = 1;
     prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
     prm.gq = static_cast<uint8_t*>(g_q);
     prm.gs = g_s;
@@ -1984,25 +1962,24 @@ extern "C" fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const voi
     CUtensorMap mp, mq;
     if (!make_map(&mp, a, M, K, 128) || !make_map(&mq, w13, 2 * I, K, 256)) return FP8_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, device_sm_count()));
-    const cudaError_t e = launch<256, kDense>(mp, mq, mp, prm, grid, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch<256, kDense, true>(mp, mq, mp, prm, grid, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
-extern "C" fp8_status fp8_moe_expert_up(const void* xq, const float* xs, int64_t T, const int32_t* row_token,
-                                        const void* w13, const float* w13_s, const int32_t* offsets, int32_t G,
-                                        int64_t R_max, void* g_q, float* g_s, int64_t I, int64_t K, int scale_fmt,
-                                        void* stream) {
+extern "C" fp8_status fp8_moe_expert_up(const void* a, const float* a_s, const void* w13, const float* w13_s,
+                                        const int32_t* offsets, int32_t G, int64_t R_max, void* g_q, float* g_s,
+                                        int64_t I, int64_t K, int scale_fmt, void* stream) {
     const fp8_status chk = swiglu_check(R_max, I, K, scale_fmt);
     if (chk != FP8_OK) return chk;
-    if (G < 0 || G > kMaxGroups || T < 0) return FP8_ERR_INVALID_ARG;
-    if (G == 0 || R_max == 0 || T == 0) return FP8_OK;
-    if (static_cast<int64_t>(G) * 2 * I > (1LL << 31) - 1 || T > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
-    if (!xq || !xs || !row_token || !w13 || !w13_s || !offsets || !g_q || !g_s || !aligned16(xq) ||
-        !aligned16(w13) || !aligned16(g_q))
+    if (G < 0 || G > kMaxGroups) return FP8_ERR_INVALID_ARG;
+    if (G == 0 || R_max == 0) return FP8_OK;
+    if (static_cast<int64_t>(G) * 2 * I > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
+    if (!a || !a_s || !w13 || !w13_s || !offsets || !g_q || !g_s || !aligned16(a) || !aligned16(w13) ||
+        !aligned16(g_q))
         return FP8_ERR_INVALID_ARG;
     if (!wide_tiles_ok()) return FP8_ERR_UNSUPPORTED;
     Params prm{};
-    prm.a_s = xs;
+    prm.a_s = a_s;
     prm.b_s = w13_s;
     prm.offsets = offsets;
     prm.M = static_cast<int>(R_max);
@@ -2011,21 +1988,18 @@ extern "C" fp8_status fp8_moe_expert_up(const void* xq, const float* xs, int64_t
     prm.NB = static_cast<int>(2 * I / 128);
     prm.G = G;
     prm.stream_k = 0;
-    prm.vec_scales = (prm.KB % 4 == 0 && aligned16(xs) && aligned16(w13_s)) ? 1 : 0;
-    prm.swiglu = 1;
+    prm.vec_scales = (prm.KB % 4 == 0 && aligned16(a_s) && aligned16(w13_s)) ? 1 : 0;
     prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
     prm.gq = static_cast<uint8_t*>(g_q);
     prm.gs = g_s;
-    prm.row_token = row_token;
 #ifdef FP8BS_TRACE_ENABLED
     prm.trace_slot = g_trace_next++ & 3;
 #endif
     CUtensorMap mp, mq;
-    // A: token rows gathered four at a time (box one row high); B: the experts' w1|w3
-    if (!make_map(&mp, xq, T, K, 1) || !make_map(&mq, w13, static_cast<int64_t>(G) * 2 * I, K, 256))
+    if (!make_map(&mp, a, R_max, K, 128) || !make_map(&mq, w13, static_cast<int64_t>(G) * 2 * I, K, 256))
         return FP8_ERR_CUDA;
     const cudaError_t e =
-        launch<256, kGrouped>(mp, mq, mp, prm, device_sm_count(), static_cast<cudaStream_t>(stream));
+        launch<256, kGrouped, true>(mp, mq, mp, prm, device_sm_count(), static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

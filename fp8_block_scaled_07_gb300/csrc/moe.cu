@@ -8,6 +8,8 @@
 //            the pairs with id == e by a block-wide ordered scan, so the
 //            result is deterministic and needs no atomics;
 //   gather   packed row r <- quantised token row row_token[r] (+ scales);
+//   quant_scatter  act_quant of each token row, written straight to its
+//            topk packed rows: act_quant and gather in one pass over x;
 //   combine  y[t] = sum_j w[t,j] * out[pair_row[t,j]] in fp32, one warp per
 //            token, 16-byte loads.
 #include "common.cuh"
@@ -91,6 +93,41 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
     }
 }
 
+// act_quant of token rows scattered to their packed rows: a half-warp per
+// 128-block of a token row (as act_quant: 16 lanes x 8 values, the block max
+// by shuffles, the library's quantisation routine), the codes and the scale
+// written to each of the token's topk packed rows pair_row[t, j].  x is read
+// once; the result equals fp8_act_quant followed by fp8_moe_gather.
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) quant_scatter_kernel(const uint4* __restrict__ x,
+                                                           const int32_t* __restrict__ pair_row, int64_t T,
+                                                           int32_t topk, int64_t K, uint2* __restrict__ aq,
+                                                           float* __restrict__ as) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
+    const int64_t KB = K / kBlock, nblocks = T * KB;
+    const int64_t hw = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 2 + half;
+    const int64_t nhw = ((static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) * 2;
+    for (int64_t blk = hw; blk < nblocks; blk += nhw) {
+        const int64_t t = blk / KB, kb = blk - t * KB;
+        float f[8];
+        unpack_bf16x8(__ldcs(x + blk * 16 + sub), f);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = block_scale(amax, UE8M0);
+        const uint2 q = quant8<UE8M0>(f, sc);
+        for (int j = 0; j < topk; ++j) {
+            const int64_t r = __ldg(pair_row + t * topk + j);
+            aq[(r * KB + kb) * 16 + sub] = q;
+            if (sub == 0) as[r * KB + kb] = sc;
+        }
+    }
+}
+
 // One warp per token; lane handles 8 consecutive columns per step.
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ out,
                                                      const float* __restrict__ w,
@@ -167,6 +204,24 @@ extern "C" fp8_status fp8_moe_gather(const void* xq, const float* xs, const int3
         return FP8_ERR_INVALID_ARG;
     gather_kernel<<<warps_grid(R), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(xq), xs, row_token, R, K, static_cast<uint4*>(aq), as);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" fp8_status fp8_moe_quant_scatter(const void* x, const int32_t* pair_row, int64_t T, int32_t topk,
+                                          int64_t K, void* aq, float* as, int scale_fmt, void* stream) {
+    if (T < 0 || topk <= 0 || K <= 0 || K % kBlock != 0) return FP8_ERR_INVALID_ARG;
+    if (scale_fmt != FP8_SCALE_FP32 && scale_fmt != FP8_SCALE_UE8M0) return FP8_ERR_INVALID_ARG;
+    if (T == 0) return FP8_OK;
+    if (!x || !pair_row || !aq || !as || !aligned16(x) || !aligned16(aq)) return FP8_ERR_INVALID_ARG;
+    const int64_t halfwarps = T * (K / kBlock);
+    const int grid = warps_grid((halfwarps + 1) / 2);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (scale_fmt == FP8_SCALE_UE8M0)
+        launch_pdl(quant_scatter_kernel<true>, dim3(grid), dim3(256), 0, st, static_cast<const uint4*>(x), pair_row,
+                   T, topk, K, static_cast<uint2*>(aq), as);
+    else
+        launch_pdl(quant_scatter_kernel<false>, dim3(grid), dim3(256), 0, st, static_cast<const uint4*>(x), pair_row,
+                   T, topk, K, static_cast<uint2*>(aq), as);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -194,21 +194,19 @@ fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const void* w13, con
                            float* g_s, int64_t M, int64_t I, int64_t K, int scale_fmt, void* stream);
 
 /* The routed experts' first half in one launch (behavior-traces page, "MoE
- * trace": tokens gathered per expert, then w2(silu(w1 x) * w3 x); source
- * tour, "Honest Limits": a fused grouped GEMM instead of the per-expert
- * loop).  Packed row r (expert g owns rows [offsets[g], offsets[g+1])) is
- * token row_token[r] of xq [T, K] e4m3 (scales xs [T, K/128]), gathered by
- * the GEMM's loads (no packed copy of the activations); each expert's w13
- * ([G, 2I, K], interleaved as for fp8_gemm_swiglu; scales [G, 2I/128,
- * K/128]) makes h1, h3, and the gate and act_quant run in the epilogue ->
- * g_q [R_max, I] e4m3, g_s [R_max, I/128] in packed row order (rows past
- * offsets[G] are not written).  offsets and row_token: int32, device.  The
- * same bytes as fp8_moe_gather + fp8_grouped_gemm + fp8_silu_mul_quant.
- * Requires I % 128 == 0, K % 128 == 0, 16-byte aligned xq, w13, g_q. */
-fp8_status fp8_moe_expert_up(const void* xq, const float* xs, int64_t T, const int32_t* row_token,
-                             const void* w13, const float* w13_s, const int32_t* offsets, int32_t G,
-                             int64_t R_max, void* g_q, float* g_s, int64_t I, int64_t K, int scale_fmt,
-                             void* stream);
+ * trace": each expert runs w2(silu(w1 x) * w3 x) on its tokens; source tour,
+ * "Honest Limits": a fused grouped GEMM instead of the per-expert loop).
+ * Expert g owns the packed rows [offsets[g], offsets[g+1]) of a [R_max, K]
+ * e4m3 (scales a_s [R_max, K/128]); its w13 ([G, 2I, K], interleaved as for
+ * fp8_gemm_swiglu; scales [G, 2I/128, K/128]) makes h1, h3, and the gate and
+ * act_quant run in the epilogue -> g_q [R_max, I] e4m3, g_s [R_max, I/128]
+ * in packed row order (rows past offsets[G] are not written).  offsets:
+ * int32 [G+1] in device memory.  The same bytes as fp8_grouped_gemm (bf16
+ * out) followed by fp8_silu_mul_quant.  Requires I % 128 == 0,
+ * K % 128 == 0, 16-byte aligned a, w13, g_q. */
+fp8_status fp8_moe_expert_up(const void* a, const float* a_s, const void* w13, const float* w13_s,
+                             const int32_t* offsets, int32_t G, int64_t R_max, void* g_q, float* g_s,
+                             int64_t I, int64_t K, int scale_fmt, void* stream);
 
 /* Expert body between the two grouped GEMMs, fused with act_quant: for
  * rows r < R and columns i < I,
@@ -238,6 +236,17 @@ fp8_status fp8_moe_route(const int32_t* ids, int64_t T, int32_t topk, int32_t E,
  * Requires K % 128 == 0 and 16-byte aligned xq, aq. */
 fp8_status fp8_moe_gather(const void* xq, const float* xs, const int32_t* row_token,
                           int64_t R, int64_t K, void* aq, float* as, void* stream);
+
+/* act_quant of the tokens written straight to their experts' packed rows
+ * (behavior-traces page, "MoE trace": each expert takes x[idx] of its
+ * tokens): row t of x [T, K] bf16 is quantised once (fp8_act_quant's rule and
+ * routine) and its codes and scales are written to packed rows
+ * pair_row[t, j], j < topk, of aq [T*topk, K] e4m3 and as [T*topk, K/128]
+ * fp32 (pair_row from fp8_moe_route).  The same bytes as fp8_act_quant
+ * followed by fp8_moe_gather, with one pass over x.  Requires K % 128 == 0,
+ * 16-byte aligned x and aq. */
+fp8_status fp8_moe_quant_scatter(const void* x, const int32_t* pair_row, int64_t T, int32_t topk, int64_t K,
+                                 void* aq, float* as, int scale_fmt, void* stream);
 
 /* Weighted combine of expert outputs (behavior-traces page, "MoE trace":
  * y[idx] += expert(x[idx]) * weight): y[t, :] = sum_j w[t, j] *

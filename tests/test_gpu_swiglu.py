@@ -3,9 +3,10 @@ epilogue (behavior-traces page, "MoE trace": w2(silu(w1 x) * w3 x); source
 tour, "FP8 with per-block scales" and "Honest Limits": the quantised input
 of w2, a fused grouped GEMM instead of the per-expert loop).
 
-fp8_gemm_swiglu and fp8_moe_expert_up must produce, bit for bit, the codes
-and scales of the unfused chain -- fp8_gemm / fp8_moe_gather +
-fp8_grouped_gemm with bf16 outputs, then fp8_silu_mul_quant -- whose stages
+fp8_gemm_swiglu and fp8_moe_expert_up (after fp8_moe_quant_scatter) must produce, bit for
+bit, the codes and scales of the unfused chain -- fp8_gemm / fp8_act_quant +
+fp8_moe_gather + fp8_grouped_gemm with bf16 outputs, then
+fp8_silu_mul_quant -- whose stages
 the other parity tests check against the oracle.  Shapes are chosen so that
 the unfused GEMM also runs whole tiles (the same fp32 summation order).  On
 top, sampled rows of g are checked against the oracle's chain (exact GEMM,
@@ -115,8 +116,13 @@ def test_moe_expert_up_matches_unfused_chain(fp8, ue8m0):
     h = fp8.fp8_grouped_gemm(aq, as_, w13, s13, off, out_bf16=True)[0]
     R = T * topk
     yq, ys, _ = fp8.fp8_silu_mul_quant(h, h[:, I:], 2 * I, R, I, fmt)
-    gq, gs = fp8.fp8_moe_expert_up(xq, xs, rtok, w13i, s13i, off, fmt)
+    # fused: act_quant + gather in one pass, then the grouped w1|w3 with the
+    # expert body in its epilogue
+    aq2, as2 = fp8.fp8_moe_quant_scatter(x, pr, fmt)
+    gq, gs = fp8.fp8_moe_expert_up(aq2, as2, w13i, s13i, off, fmt)
     fp8.fp8_device_status()
+    assert np.array_equal(host_bits(aq2), host_bits(aq)), "quant_scatter codes differ from act_quant + gather"
+    assert np.array_equal(host_f32(as2).view(np.uint32), host_f32(as_).view(np.uint32)), "quant_scatter scales"
     offs = off.cpu().numpy()
     counts = np.diff(offs)
     assert counts.min() == 0 and counts.max() > 128 and np.any((counts > 0) & (counts < 128))
