@@ -6,7 +6,7 @@ with bf16 activations ~N(0,1) (0.5% outliers x30) and e4m3 weights with
 128x128 fp32 block scales drawn from N(0, 0.02).  One step = act_quant +
 fp8_gemm for each of the three layers, i.e. one fp8_linear call per layer,
 each one kernel at this batch (the quantisation runs inside the GEMM) --
-three launches per step, replayed from CUDA graphs of four consecutive
+three launches per step, replayed from CUDA graphs of twenty consecutive
 steps.  Four weight sets (4 x 167 MB) rotate between steps so every step
 streams its weights from HBM (inputs larger than L2).
 
@@ -53,6 +53,7 @@ import synthetic as syn  # noqa: E402
 
 M_DECODE = 16
 ROTATIONS = 4
+GRAPH_STEPS = 20
 LAYERS = list(syn.DECODE_LAYERS)      # wq_a, wq_b, wo
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -792,18 +793,19 @@ def main():
 
     # one graph per weight rotation; nothing but the step's kernels, so the
     # programmatic launch edges between consecutive kernels stay intact
-    # one graph holds R consecutive steps (the R weight rotations in turn),
-    # as a decode loop captures many layers in one graph: inside it
-    # consecutive kernels keep their programmatic launch edges.  K steps =
-    # K // R replays of it plus K % R single-step graphs.
-    graph_r = capture(torch, lambda: [dec.step(r) for r in range(dec.R)])
+    # one graph holds GRAPH_STEPS consecutive steps (the weight rotations in
+    # turn), as a decode engine captures its whole forward pass in one graph:
+    # inside it consecutive kernels keep their programmatic launch edges.  K
+    # steps = K // GRAPH_STEPS replays of it plus K % GRAPH_STEPS single-step
+    # graphs.
+    graph_r = capture(torch, lambda: [dec.step(i % dec.R) for i in range(GRAPH_STEPS)])
     graphs = [capture(torch, lambda r=r: dec.step(r)) for r in range(dec.R)]
 
     def run_steps(n):
-        for _ in range(n // dec.R):
+        for _ in range(n // GRAPH_STEPS):
             graph_r.replay()
-        for i in range(n % dec.R):
-            graphs[i].replay()
+        for i in range(n % GRAPH_STEPS):
+            graphs[i % dec.R].replay()
     run_steps(args.warmup)
     torch.cuda.synchronize()
     fp8.fp8_device_status()
@@ -811,6 +813,8 @@ def main():
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
+    run_steps(args.warmup)   # (again: the GPU idled while the sampler started)
+    torch.cuda.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
@@ -943,7 +947,7 @@ def main():
                                "layer, the quantisation inside the GEMM)",
                    "global_batch": M * world, "parallelism": f"replicas x{world}",
                    "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
-                   "launch": f"CUDA graphs of {dec.R} steps each (programmatic launch between kernels)"},
+                   "launch": f"CUDA graphs of {GRAPH_STEPS} steps each (programmatic launch between kernels)"},
         "tflops": world * step_flops / (ms_per_step * 1e9),
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,

@@ -19,10 +19,10 @@
 //     row (st.async, counted as transaction bytes on the owner's barrier) --
 //     and the owner sums them in rank order (deterministic).
 //   * One 128-K slab per pipeline stage, three stages, so 2-3 CTAs fit on an
-//     SM, and the plan gives a launch about half of the CTA slots: with
-//     programmatic dependent launch the next launch's CTAs are all resident,
-//     set up and prefetching their first weight slabs into L2 while this one
-//     runs, and they all pass griddepcontrol.wait together.
+//     SM, and a 16-token launch takes about three quarters of the CTA slots:
+//     with programmatic dependent launch most of the next launch's CTAs are
+//     resident, set up and prefetching their first weight slabs into L2
+//     while this one runs, and they pass griddepcontrol.wait together.
 //   * Four "activation" warps feed the token side of each slab: they load
 //     their values from global memory one slab ahead, quantise them (fused;
 //     the library's act_quant routine) or take the e4m3 codes as they are,
@@ -70,31 +70,25 @@ constexpr int kDecMaxCluster = 16;
 #define FP8BS_DEC_EVICT_FIRST 1   // weight loads marked evict-first in L2 (each byte is read once)
 #endif
 
-#ifndef FP8BS_DEC_S16
-#define FP8BS_DEC_S16 3   // pipeline stages of the 16-, 32- and 64-token kernels
-#endif
-#ifndef FP8BS_DEC_S32
-#define FP8BS_DEC_S32 3
-#endif
-#ifndef FP8BS_DEC_S64
-#define FP8BS_DEC_S64 3
-#endif
+constexpr int kDecStages = 3;   // pipeline stages (one 128-K slab each)
 // Percent of the device's CTA slots one launch may take.  16-token tiles
-// (three CTAs per SM): half, so the next launch's CTAs are resident and
-// waiting when this one ends (measured on GB300, decode step at M = 16:
-// 40.9 us at half against 50.4 us at all slots); 32- and 64-token tiles (two
-// per SM): all, their streams need the bytes in flight (M = 64: 74.1 us
-// against 85.4 us).
+// (three CTAs per SM): three quarters -- enough bytes in flight for the
+// long weight streams, and room left for most of the next launch's CTAs to
+// be resident and waiting when this one ends (measured on GB300, decode
+// step at M = 16 / the wo layer alone, back to back: 50% 41.4 / 28.2 us,
+// 60% 41.4 / 28.2, 66% 42.7 / 24.6, 75% 40.0 / 22.7, 100% 50.4 / 29.7);
+// 32- and 64-token tiles (two per SM): all, their streams need the bytes in
+// flight (M = 64: 74.1 us against 85.4 us at half).
 #ifndef FP8BS_DEC_FILL16
-#define FP8BS_DEC_FILL16 50
+#define FP8BS_DEC_FILL16 75
 #endif
 #ifndef FP8BS_DEC_FILL
 #define FP8BS_DEC_FILL 100
 #endif
 
-template <int BN>
+template <int BN, int S>
 struct Dec {
-    static constexpr int kStages = BN == 16 ? FP8BS_DEC_S16 : (BN == 32 ? FP8BS_DEC_S32 : FP8BS_DEC_S64);
+    static constexpr int kStages = S;
     static constexpr int kWBytes = 128 * kBlock;           // weight slab: 128 rows x 128 e4m3
     static constexpr int kXBytes = BN * kBlock;            // token codes of a slab
     static constexpr int kRing = kStages + 2;              // scale-product slots (see the act role)
@@ -138,11 +132,11 @@ __device__ __forceinline__ bool dec_warp_all(bool ok) { return __all_sync(0xFFFF
 // First row owned by cluster rank o when c CTAs share 128 rows: ceil(128 o / c).
 __device__ __forceinline__ int own_lo(int o, int c) { return (o * 128 + c - 1) / c; }
 
-template <int BN, bool FUSED>
-__global__ void __launch_bounds__(kDecThreads, Dec<BN>::kMinBlocks)
+template <int BN, bool FUSED, int SS>
+__global__ void __launch_bounds__(kDecThreads, (Dec<BN, SS>::kMinBlocks))
     decode_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                   const DecParams p) {
-    using D = Dec<BN>;
+    using D = Dec<BN, SS>;
     constexpr int S = D::kStages, R = D::kRing;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -485,33 +479,34 @@ __global__ void __launch_bounds__(kDecThreads, Dec<BN>::kMinBlocks)
 }
 
 // ------------------------------------------------------------------ host side
-template <int BN, bool FUSED>
+template <int BN, bool FUSED, int S>
 bool configure(int dev) {
     static int done[64] = {0};   // 1 configured, 2 failed
     if (dev < 0 || dev >= 64) return false;
     if (done[dev] == 0) {
-        const auto fn = decode_kernel<BN, FUSED>;
-        const bool ok = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Dec<BN>::kSmemBytes) ==
-                            cudaSuccess &&
-                        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        const auto fn = decode_kernel<BN, FUSED, S>;
+        const bool ok =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Dec<BN, S>::kSmemBytes) ==
+                cudaSuccess &&
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         done[dev] = ok ? 1 : 2;
     }
     return done[dev] == 1;
 }
 
 // Largest cluster size (<= 16) the device can schedule for this kernel.
-template <int BN, bool FUSED>
+template <int BN, bool FUSED, int S>
 int max_cluster(int dev) {
     static int cache[64] = {0};
     if (dev < 0 || dev >= 64) return 8;
     if (cache[dev] == 0) {
         int best = 1;
-        if (configure<BN, FUSED>(dev)) {
+        if (configure<BN, FUSED, S>(dev)) {
             for (int cl = kDecMaxCluster; cl >= 2; --cl) {
                 cudaLaunchConfig_t cfg = {};
                 cfg.gridDim = dim3(cl);
                 cfg.blockDim = dim3(kDecThreads);
-                cfg.dynamicSmemBytes = Dec<BN>::kSmemBytes;
+                cfg.dynamicSmemBytes = Dec<BN, S>::kSmemBytes;
                 cudaLaunchAttribute attr;
                 attr.id = cudaLaunchAttributeClusterDimension;
                 attr.val.clusterDim.x = cl;
@@ -520,7 +515,7 @@ int max_cluster(int dev) {
                 cfg.attrs = &attr;
                 cfg.numAttrs = 1;
                 int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<BN, FUSED>, &cfg) == cudaSuccess && n > 0) {
+                if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<BN, FUSED, S>, &cfg) == cudaSuccess && n > 0) {
                     best = cl;
                     break;
                 }
@@ -533,7 +528,7 @@ int max_cluster(int dev) {
 }
 
 struct DecPlan {
-    int bn, tiles, c, grid;
+    int bn, stages, tiles, c, grid;
 };
 
 int current_device() {
@@ -543,16 +538,8 @@ int current_device() {
 }
 
 // c: the fewest CTAs per tile that minimise the slabs of the busiest CTA,
-// within about half the CTA slots of the device (the other half is for the
-// next launch, whose CTAs then wait resident) and the cluster limit.
-DecPlan decode_plan(int64_t M, int64_t N, int64_t K, int sms, int cmax) {
-    DecPlan pl{};
-    pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-    pl.tiles = static_cast<int>((N + 127) / 128);
-    const int KB = static_cast<int>(K / kBlock);
-    const int per_sm = pl.bn == 16 ? Dec<16>::kMinBlocks : (pl.bn == 32 ? Dec<32>::kMinBlocks : Dec<64>::kMinBlocks);
-    const int fill = pl.bn == 16 ? FP8BS_DEC_FILL16 : FP8BS_DEC_FILL;
-    const long long budget = std::max<long long>(1, static_cast<long long>(sms) * per_sm * fill / 100);
+// within the launch's share of the device's CTA slots and the cluster limit.
+void plan_split(DecPlan& pl, int KB, long long budget, int cmax) {
     int best_c = 1, best_max = KB;
     for (int c = 2; c <= std::min(cmax, KB); ++c) {
         if (static_cast<long long>(pl.tiles) * c > budget) break;
@@ -564,24 +551,36 @@ DecPlan decode_plan(int64_t M, int64_t N, int64_t K, int sms, int cmax) {
     }
     pl.c = best_c;
     pl.grid = pl.tiles * best_c;
+}
+
+DecPlan decode_plan(int64_t M, int64_t N, int64_t K, int sms, int cmax) {
+    DecPlan pl{};
+    pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    pl.tiles = static_cast<int>((N + 127) / 128);
+    pl.stages = kDecStages;
+    const int KB = static_cast<int>(K / kBlock);
+    const int per_sm = pl.bn == 16 ? Dec<16, kDecStages>::kMinBlocks
+                                   : (pl.bn == 32 ? Dec<32, kDecStages>::kMinBlocks : Dec<64, kDecStages>::kMinBlocks);
+    const int fill = pl.bn == 16 ? FP8BS_DEC_FILL16 : FP8BS_DEC_FILL;
+    plan_split(pl, KB, std::max<long long>(1, static_cast<long long>(sms) * per_sm * fill / 100), cmax);
     return pl;
 }
 
-template <int BN, bool FUSED>
+template <int BN, bool FUSED, int S>
 cudaError_t launch_decode(const CUtensorMap& tw, const CUtensorMap& tx, const DecParams& prm, int grid,
                           unsigned cluster, cudaStream_t st) {
     const int dev = current_device();
-    if (!configure<BN, FUSED>(dev)) return cudaErrorInvalidValue;
-    return launch_pdl_cluster(decode_kernel<BN, FUSED>, dim3(grid), dim3(kDecThreads), Dec<BN>::kSmemBytes, st,
-                              cluster, tw, tx, prm);
+    if (!configure<BN, FUSED, S>(dev)) return cudaErrorInvalidValue;
+    return launch_pdl_cluster(decode_kernel<BN, FUSED, S>, dim3(grid), dim3(kDecThreads), Dec<BN, S>::kSmemBytes,
+                              st, cluster, tw, tx, prm);
 }
 
 // (the fused and plain kernels of a tile width need the same resources, so
 // one query serves both and their plans agree)
 int plan_cmax(int bn, int dev) {
-    if (bn == 16) return max_cluster<16, false>(dev);
-    if (bn == 32) return max_cluster<32, false>(dev);
-    return max_cluster<64, false>(dev);
+    if (bn == 16) return max_cluster<16, false, kDecStages>(dev);
+    if (bn == 32) return max_cluster<32, false, kDecStages>(dev);
+    return max_cluster<64, false, kDecStages>(dev);
 }
 
 #ifdef FP8BS_TRACE_ENABLED
@@ -628,12 +627,12 @@ fp8_status decode_gemm(const void* x, const void* xq, const float* a_s, const vo
     const unsigned cl = static_cast<unsigned>(pl.c);
     cudaError_t e;
     if (pl.bn == 16)
-        e = fused ? launch_decode<16, true>(tw, tx, prm, pl.grid, cl, st)
-                  : launch_decode<16, false>(tw, tx, prm, pl.grid, cl, st);
+        e = fused ? launch_decode<16, true, kDecStages>(tw, tx, prm, pl.grid, cl, st)
+                  : launch_decode<16, false, kDecStages>(tw, tx, prm, pl.grid, cl, st);
     else if (pl.bn == 32)
-        e = launch_decode<32, false>(tw, tx, prm, pl.grid, cl, st);
+        e = launch_decode<32, false, kDecStages>(tw, tx, prm, pl.grid, cl, st);
     else
-        e = launch_decode<64, false>(tw, tx, prm, pl.grid, cl, st);
+        e = launch_decode<64, false, kDecStages>(tw, tx, prm, pl.grid, cl, st);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

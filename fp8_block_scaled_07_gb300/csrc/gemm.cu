@@ -82,17 +82,14 @@ constexpr size_t kCounterBytes = kMaxSkTiles * sizeof(int);
 
 enum Variant { kDense = 0, kGrouped = 2 };
 
-// Register split of the 128x256 kernels (warpgroup 0 / epilogue warpgroups)
-// and the width of the epilogue's TMEM loads (columns per tcgen05.ld).
+// Register split of the 128x256 kernels (warpgroup 0 / epilogue warpgroups).
 #ifndef FP8BS_REGS_LOW
 #define FP8BS_REGS_LOW 120
 #endif
 #ifndef FP8BS_REGS_HIGH
 #define FP8BS_REGS_HIGH 192
 #endif
-#ifndef FP8BS_EPI_LD
-#define FP8BS_EPI_LD 32
-#endif
+
 
 struct Params {
     const float* a_s;          // [rows_a, KB]
@@ -135,7 +132,7 @@ struct Seg {
     int tile, k0, k1;
 };
 
-template <int BN, int V>
+template <int BN, int V, bool SW = false>
 struct Cfg {
     static constexpr int kQTileBytes = BN * kBlock;
     static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
@@ -146,7 +143,7 @@ struct Cfg {
     static constexpr int kThreads = 128 + 32 * kEpiWarps;
     static constexpr int kMinBlocks = 1;
     static constexpr int kCPT = BN * 4 / kEpiWarps;   // accumulator columns per epilogue thread
-    static constexpr bool kSplitRegs = kEpiWarps == 8;
+    static constexpr bool kSplitRegs = BN == 256;
     // the MMA issuer checks one barrier per slab (each check by the issuing
     // thread costs tensor time): a stage's full barrier also counts the
     // epilogue warps' release of the TMEM buffer the slab will write, i.e. of
@@ -538,14 +535,6 @@ __device__ __forceinline__ void promote(uint32_t taddr, float (&acc)[BN], const 
         tmem_ld16(taddr, r);
         tmem_wait_ld();
         fma_chunk<16, PER_COL>(acc, r, sc_col, sc);
-    } else if constexpr (FP8BS_EPI_LD == 64 && BN % 64 == 0) {
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-            uint32_t r[64];
-            tmem_ld64(taddr + c0, r);
-            tmem_wait_ld();
-            fma_chunk<64, PER_COL>(acc + c0, r, PER_COL ? sc_col + c0 : nullptr, sc);
-        }
     } else {
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -574,10 +563,10 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const v
 // SW: the expert body fused into the epilogue (a kernel of its own, so
 // that the plain kernels' register allocation does not carry it)
 template <int BN, int V, bool SW>
-__global__ void __launch_bounds__((Cfg<BN, V>::kThreads), (Cfg<BN, V>::kMinBlocks))
+__global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::kMinBlocks))
     gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_c, const Params p) {
-    using C = Cfg<BN, V>;
+    using C = Cfg<BN, V, SW>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1657,7 +1646,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int sms) {
 template <int BN, int V, bool SW = false>
 cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorMap& mc, const Params& prm,
                    int grid, cudaStream_t st) {
-    using C = Cfg<BN, V>;
+    using C = Cfg<BN, V, SW>;
     constexpr int smem = C::kSmemBytes;
     static int configured[64] = {0};
     int dev = 0;
@@ -1676,7 +1665,7 @@ cudaError_t launch(const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorM
 // split assumes (launch total >= the sum of the new per-warpgroup counts).
 template <int V, bool SW>
 bool split_regs_ok() {
-    using C = Cfg<256, V>;
+    using C = Cfg<256, V, SW>;
     cudaFuncAttributes a{};
     if (cudaFuncGetAttributes(&a, gemm_kernel<256, V, SW>) != cudaSuccess) return false;
     return a.numRegs * C::kThreads >= C::kRegsLow * 128 + C::kRegsHigh * 32 * C::kEpiWarps;
@@ -1810,9 +1799,10 @@ extern "C" fp8_status fp8_gemm(const void* a, const float* a_s, const void* b, c
     CUtensorMap mp, mq, mc;
     // P: 128-row tiles of the activations; Q: BN-row tiles of the weight
     if (!make_map(&mp, a, M, K, 128) || !make_map(&mq, b, N, K, pl.bn)) return FP8_ERR_CUDA;
-    // C (bf16 only, 16-byte rows): 32 x 64 boxes for the TMA tile store
+    // C (bf16 only, 16-byte rows): staging-box-high x 64 boxes for the TMA tile store
     prm.tma_store = (c_bf16 && !c_fp32 && N % 8 == 0) ? 1 : 0;
-    if (prm.tma_store && !make_map_bf16(&mc, c_bf16, M, N, 32)) return FP8_ERR_CUDA;
+    const int box_rows = pl.bn == 256 ? Cfg<256, kDense>::kStgRows : Cfg<128, kDense>::kStgRows;
+    if (prm.tma_store && !make_map_bf16(&mc, c_bf16, M, N, box_rows)) return FP8_ERR_CUDA;
     if (!prm.tma_store) mc = mp;   // not read
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e = pl.bn == 256 ? launch<256, kDense>(mp, mq, mc, prm, pl.grid, st)
