@@ -164,8 +164,6 @@ struct Cfg {
     static constexpr int kStgBytes = kEpiWarps * kStgRows * 128;
     static constexpr int kSmemBytes =
         1024 /*align slack*/ + kStages * kStageBytes + kStgBytes + kBarBytes + kExtraBytes;
-    // weight slabs each CTA prefetches into L2 before its inputs are ready
-    static constexpr int kL2Prefetch = kStages;
 };
 
 // ------------------------------------------------------------------ schedule
@@ -615,19 +613,6 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_p);
         tma_prefetch_desc(&tm_q);
-        if constexpr (V != kGrouped) {
-            // start streaming this CTA's first weight slabs into L2 while the
-            // producer of the activations may still be running
-            SegIter pit;
-            pit.init(p, p.num_tiles);
-            Seg ps;
-            int n = 0;
-            while (n < C::kL2Prefetch && pit.next(ps)) {
-                const Tile tg = tile_geom<BN, V>(p, ps.tile, nullptr);
-                for (int kb = ps.k0; kb < ps.k1 && n < C::kL2Prefetch; ++kb, ++n)
-                    tma_prefetch_l2_2d(&tm_q, kb * kBlock, tg.q_row0);
-            }
-        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, C::kTmemCols);
