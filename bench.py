@@ -390,6 +390,22 @@ def decode_rows(fp8, torch, dec, hbm, out):
                                    "kernels": 1 if fused else 2}
             del g
 
+        # the MLA query projections chained: wq_b reads wq_a's output (as a
+        # decoder does, minus the norm between them), back to back on the
+        # stream, against the two layers timed apart
+        ya = torch.empty((M, syn.DECODE_LAYERS["wq_a"][0]), dtype=torch.bfloat16, device=dev)
+
+        def chain():
+            for r in range(dec.R):
+                (qa, sa), (qb, sb) = dec.w[r]["wq_a"], dec.w[r]["wq_b"]
+                fp8.fp8_linear(xs[r]["wq_a"], qa, sa, c_bf16=ya, workspace=ws)
+                fp8.fp8_linear(ya, qb, sb, c_bf16=ys["wq_b"], workspace=ws)
+        g = capture(torch, chain)
+        t = time_windows(torch, g, 50)
+        row["chain_wq_a_wq_b"] = {"us": t["median"] / dec.R * 1e3,
+                                  "separate_us": row["layers"]["wq_a"]["us"] + row["layers"]["wq_b"]["us"]}
+        del g, ya
+
         def steps():
             for r in range(dec.R):
                 for name in LAYERS:

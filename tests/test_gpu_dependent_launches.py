@@ -107,3 +107,41 @@ def test_linear_reads_activations_written_just_before(fp8):
         torch.cuda.synchronize()
         assert torch.equal(chained[i].view(torch.int16), settled.view(torch.int16)), f"round {i}: stale inputs read"
     fp8.fp8_device_status()
+
+
+def test_query_projection_chain(fp8):
+    # wq_a -> wq_b at a decode batch, as a decoder chains them (minus the
+    # norm in between): the second fused linear quantises the first one's
+    # bf16 output, launched right behind it, round after round with one
+    # output buffer.  Each round must equal the settled chain bit for bit and
+    # match the oracle's chain (exact GEMM, bf16 rounding, act_quant, GEMM).
+    import oracle
+    from tests.helpers import check_gemm, host_bits, host_f32
+
+    M = 16
+    (Na, Ka), (Nb, Kb) = syn.DECODE_LAYERS["wq_a"], syn.DECODE_LAYERS["wq_b"]
+    wa, wa_s = fp8.fp8_weight_quant(syn.normal_bf16_device((Na, Ka), 0.02, 540, "cuda"))
+    wb, wb_s = fp8.fp8_weight_quant(syn.normal_bf16_device((Nb, Kb), 0.02, 541, "cuda"))
+    xs = [syn.normal_bf16_device((M, Ka), 1.0, 542 + i, "cuda") for i in range(3)]
+    ya = torch.empty((M, Na), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    chained = []
+    for x in xs:
+        fp8.fp8_linear(x, wa, wa_s, c_bf16=ya)
+        chained.append(fp8.fp8_linear(ya, wb, wb_s, out_fp32=True))
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+    wa_h, wa_sh, wb_h, wb_sh = host_bits(wa), host_f32(wa_s), host_bits(wb), host_f32(wb_s)
+    for i, x in enumerate(xs):
+        y1 = fp8.fp8_linear(x, wa, wa_s)[0]
+        torch.cuda.synchronize()
+        sb, sf = fp8.fp8_linear(y1, wb, wb_s, out_fp32=True)
+        torch.cuda.synchronize()
+        cb, cf = chained[i]
+        assert torch.equal(cb.view(torch.int16), sb.view(torch.int16)), f"round {i}: stale activations read"
+        assert torch.equal(cf.view(torch.int32), sf.view(torch.int32)), f"round {i}: stale activations read"
+        # the oracle's chain from the same first-layer output
+        aq, as_ = oracle.act_quant(host_bits(y1))
+        ref, mag = oracle.gemm(aq, as_, wb_h, wb_sh)
+        check_gemm(ref, mag, host_f32(cf), host_bits(cb), f"round {i}: wq_b after wq_a")
+    fp8.fp8_device_status()
