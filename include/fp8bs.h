@@ -259,7 +259,9 @@ fp8_status fp8_moe_combine(const void* out, const float* w, const int32_t* pair_
  * status words: FP8_ERR_TIMEOUT if a kernel's bounded wait gave up since
  * the last call, FP8_ERR_INVALID_ARG if fp8_gemm_ue8m0 met a scale that is
  * not a power of two, FP8_ERR_CUDA if the stream reported an error, else
- * FP8_OK. */
+ * FP8_OK.  After FP8_ERR_TIMEOUT the outputs of the calls since the last
+ * check are unspecified, and so are the split-tile counters of the
+ * workspaces they used: zero those workspaces again before reusing them. */
 fp8_status fp8_device_status(void* stream);
 
 /* Test hooks of the failure path (no counterpart in the pages: they exist so
