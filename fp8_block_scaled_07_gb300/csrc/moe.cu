@@ -4,9 +4,11 @@
 // and add its output times the gate weight back into y).
 //
 //   route    stable counting sort of (token, slot) pairs by expert id; CTA e
-//            counts the pairs with id < e (its first packed row) and ranks
-//            the pairs with id == e by a block-wide ordered scan, so the
-//            result is deterministic and needs no atomics;
+//            counts, each warp over a contiguous range read 32 pairs at a
+//            time, the pairs with id < e (its first packed row) and those
+//            with id == e, and ranks the latter in pair order (warp ballots,
+//            then the warps' counts in order), so the result is
+//            deterministic and needs no atomics;
 //   gather   packed row r <- quantised token row row_token[r] (+ scales);
 //   quant_scatter  act_quant of each token row, written straight to its
 //            topk packed rows: act_quant and gather in one pass over x;
@@ -26,49 +28,55 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t* __r
                                                               int32_t* __restrict__ row_token) {
     griddep_launch_dependents();
     griddep_wait();
-    __shared__ int warp_cnt[kRouteThreads / 32];
-    __shared__ int warp_lt[kRouteThreads / 32];
-    __shared__ int s_base;
+    constexpr int kWarps = kRouteThreads / 32;
+    __shared__ int s_lt[kWarps];
+    __shared__ int s_eq[kWarps];
     const int e = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // pass 1: number of pairs with id < e  -> first packed row of expert e
-    int lt = 0;
-    for (int64_t i = threadIdx.x; i < P; i += kRouteThreads) lt += (__ldg(ids + i) < e) ? 1 : 0;
+    // warp w owns the contiguous pairs [lo, hi) (a multiple of 32 long),
+    // read 32 at a time: one pass counts the pairs with id < e (expert e's
+    // first packed row) and those with id == e
+    const int64_t seg = ((P + kWarps - 1) / kWarps + 31) / 32 * 32;
+    const int64_t lo = min(P, seg * warp), hi = min(P, lo + seg);
+    int lt = 0, eq = 0;
+    // (unrolled: eight loads in flight per lane, not one L2 round trip per step)
+#pragma unroll 8
+    for (int64_t i0 = lo; i0 < hi; i0 += 32) {
+        const int64_t i = i0 + lane;
+        const int v = i < hi ? __ldg(ids + i) : -1;
+        lt += (i < hi && v < e) ? 1 : 0;
+        eq += __popc(__ballot_sync(0xFFFFFFFFu, v == e));
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) lt += __shfl_xor_sync(0xFFFFFFFFu, lt, o);
-    if (lane == 0) warp_lt[warp] = lt;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int s = 0;
-        for (int w = 0; w < kRouteThreads / 32; ++w) s += warp_lt[w];
-        s_base = s;
-        offsets[e] = s;
-        if (e == E - 1) offsets[E] = static_cast<int32_t>(P);
+    if (lane == 0) {
+        s_lt[warp] = lt;
+        s_eq[warp] = eq;
     }
     __syncthreads();
-    int base = s_base;
-    // pass 2: ordered ranks of the pairs with id == e
-    for (int64_t c0 = 0; c0 < P; c0 += kRouteThreads) {
-        const int64_t i = c0 + threadIdx.x;
-        const bool hit = i < P && __ldg(ids + i) == e;
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, hit);
-        const int before_in_warp = __popc(ball & ((1u << lane) - 1u));
-        if (lane == 0) warp_cnt[warp] = __popc(ball);
-        __syncthreads();
-        int before = base + before_in_warp;
-        int total = 0;
+    int base = 0, before = 0;
 #pragma unroll
-        for (int w = 0; w < kRouteThreads / 32; ++w) {
-            const int c = warp_cnt[w];
-            if (w < warp) before += c;
-            total += c;
-        }
+    for (int w = 0; w < kWarps; ++w) {
+        base += s_lt[w];
+        if (w < warp) before += s_eq[w];
+    }
+    if (threadIdx.x == 0) {
+        offsets[e] = base;
+        if (e == E - 1) offsets[E] = static_cast<int32_t>(P);
+    }
+    // the pairs with id == e take packed rows base + rank, in pair order
+    int r = base + before;
+#pragma unroll 8
+    for (int64_t i0 = lo; i0 < hi; i0 += 32) {
+        const int64_t i = i0 + lane;
+        const bool hit = i < hi && __ldg(ids + i) == e;
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, hit);
         if (hit) {
-            pair_row[i] = before;
-            row_token[before] = static_cast<int32_t>(i / topk);
+            const int row = r + __popc(ball & ((1u << lane) - 1u));
+            pair_row[i] = row;
+            row_token[row] = static_cast<int32_t>(i / topk);
         }
-        base += total;
-        __syncthreads();
+        r += __popc(ball);
     }
 }
 
@@ -128,7 +136,11 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint4* __restr
     }
 }
 
-// One warp per token; lane handles 8 consecutive columns per step.
+// One warp per token; lane handles 8 consecutive columns per step.  TK > 0
+// is the topk known at compile time: the token's rows and weights are read
+// once and its TK row loads of a step are all in flight together (the same
+// fp32 sums, in the same slot order, as the generic loop).
+template <int TK>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ out,
                                                      const float* __restrict__ w,
                                                      const int32_t* __restrict__ pair_row,
@@ -141,18 +153,36 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t chunks = D / 8;
+    auto add = [](float (&acc)[8], float wj, const uint4& v) {
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj, __uint_as_float(u[i] << 16), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        }
+    };
     for (int64_t t = warp; t < T; t += nwarps) {
+        int64_t rows[TK > 0 ? TK : 1];
+        float wts[TK > 0 ? TK : 1];
+        if constexpr (TK > 0) {
+#pragma unroll
+            for (int j = 0; j < TK; ++j) {
+                rows[j] = __ldg(pair_row + t * TK + j);
+                wts[j] = __ldg(w + t * TK + j);
+            }
+        }
         for (int64_t c = lane; c < chunks; c += 32) {
             float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int j = 0; j < topk; ++j) {
-                const int64_t r = __ldg(pair_row + t * topk + j);
-                const float wj = __ldg(w + t * topk + j);
-                const uint4 v = __ldcs(out + r * chunks + c);
-                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+            if constexpr (TK > 0) {
+                uint4 v[TK];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = fmaf(wj, __uint_as_float(u[i] << 16), acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(wj, __uint_as_float(u[i] & 0xFFFF0000u), acc[2 * i + 1]);
+                for (int j = 0; j < TK; ++j) v[j] = __ldcs(out + rows[j] * chunks + c);
+#pragma unroll
+                for (int j = 0; j < TK; ++j) add(acc, wts[j], v[j]);
+            } else {
+                for (int j = 0; j < topk; ++j) {
+                    const int64_t r = __ldg(pair_row + t * topk + j);
+                    add(acc, __ldg(w + t * topk + j), __ldcs(out + r * chunks + c));
                 }
             }
             if (y_bf16) {
@@ -233,7 +263,8 @@ extern "C" fp8_status fp8_moe_combine(const void* out, const float* w, const int
     if (!out || !w || !pair_row || (!y_bf16 && !y_fp32) || !aligned16(out) ||
         (y_bf16 && !aligned16(y_bf16)) || (y_fp32 && !aligned16(y_fp32)))
         return FP8_ERR_INVALID_ARG;
-    combine_kernel<<<warps_grid(T), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    auto kernel = topk == 8 ? combine_kernel<8> : combine_kernel<0>;   // (the V3 routing: top-8)
+    kernel<<<warps_grid(T), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(out), w, pair_row, T, topk, D, static_cast<uint4*>(y_bf16),
         reinterpret_cast<float4*>(y_fp32));
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
