@@ -126,11 +126,11 @@ fp8_status fp8_gemm_ue8m0(const void* a, const float* a_s, const void* b, const 
  * weight and its block scales).  x [M, K] bf16 (device), w [N, K] e4m3,
  * w_s [ceil(N/128), K/128] fp32 -> c_bf16 and/or c_fp32 [M, N].  scale_fmt
  * is the activation scale format.  The result equals fp8_act_quant followed
- * by fp8_gemm bit for bit.  For M <= 16 on decode shapes whose K is split
- * into short ranges per CTA the quantisation runs inside the GEMM kernel (no
- * workspace); otherwise the activation codes and scales are staged in the
- * workspace, whose size
- * fp8_linear_workspace_size() gives (0 when none is needed).  Layout:
+ * by fp8_gemm bit for bit.  For M <= 16 the quantisation runs inside the
+ * decode GEMM kernel (one kernel, no workspace); otherwise the activation
+ * codes and scales are staged in the workspace first (act_quant, then the
+ * GEMM), whose size fp8_linear_workspace_size() gives (0 when none is
+ * needed).  Layout:
  * fp8_gemm's workspace first (same zero-fill rule, and never shorter than
  * its 16 KiB of split-tile counters), then codes and scales, so one
  * workspace can serve both entry points and any shapes in stream order. */
