@@ -754,7 +754,29 @@ def _ncu_dequant(fp8, torch):
     fp8.fp8_device_status()
 
 
+def _ncu_moe(fp8, torch, which):
+    # the MoE workload at a quarter of its experts, sized for ncu: 1024 tokens
+    # x top-8 of 64 experts (Zipf), so 128 rows per expert on average as in
+    # the 4096 x 256 case; random e4m3 codes and scales in [0.5, 1.5)
+    T, E, K8, D, I = 1024, 64, syn.MOE_TOPK, syn.MOE_DIM, syn.MOE_INTER
+    rt = syn.moe_routing(T=T, E=E, topk=K8)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(6)
+    N, K = (2 * I, D) if which == "w13" else (D, I)
+    b = _ncu_rand_e4m3(torch, (E, N, K), gen)
+    b_s = torch.rand((E, N // 128, K // 128), device="cuda", generator=gen) + 0.5
+    off, _, _ = fp8.fp8_moe_route(torch.from_numpy(rt.ids).cuda(), E)
+    a = _ncu_rand_e4m3(torch, (T * K8, K), gen)
+    a_s = torch.rand((T * K8, K // 128), device="cuda", generator=gen) + 0.5
+    for _ in range(3):
+        fp8.fp8_grouped_gemm(a, a_s, b, b_s, off)
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+
 NCU_CASES = {
+    "moe_w13": lambda fp8, torch: _ncu_moe(fp8, torch, "w13"),
+    "moe_w2": lambda fp8, torch: _ncu_moe(fp8, torch, "w2"),
     "decode_wo": lambda fp8, torch: _ncu_gemm(fp8, torch, 16, *syn.DECODE_LAYERS["wo"]),
     "decode_wq_a_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wq_a"]),
     "decode_wq_b_linear": lambda fp8, torch: _ncu_linear(fp8, torch, 16, *syn.DECODE_LAYERS["wq_b"]),
