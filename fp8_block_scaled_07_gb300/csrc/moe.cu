@@ -3,12 +3,13 @@
 // the tokens per expert, take each expert's tokens in order, run the expert
 // and add its output times the gate weight back into y).
 //
-//   route    stable counting sort of (token, slot) pairs by expert id; CTA e
-//            counts, each warp over a contiguous range read 32 pairs at a
-//            time, the pairs with id < e (its first packed row) and those
-//            with id == e, and ranks the latter in pair order (warp ballots,
-//            then the warps' counts in order), so the result is
-//            deterministic and needs no atomics;
+//   route    stable counting sort of (token, slot) pairs by expert id; each
+//            CTA owns a group of experts and reads the ids twice (16-byte
+//            loads where they allow it): once to count, per warp, the pairs
+//            below its group and those of each of its experts, once to
+//            rank its experts' pairs in pair order (warp match groups, then
+//            the warps' counts in order), so the result is deterministic
+//            and needs no global atomics;
 //   gather   packed row r <- quantised token row row_token[r] (+ scales);
 //   quant_scatter  act_quant of each token row, written straight to its
 //            topk packed rows: act_quant and gather in one pass over x;
@@ -19,64 +20,138 @@
 namespace fp8bs {
 namespace {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteMaxOwn = 32;   // experts per CTA (E <= 1024 over at most 32 CTAs)
 
+// CTA c owns experts [e0, e0 + ne).  Each warp takes a contiguous range of
+// the pairs; one pass counts, per warp, the pairs with id < e0 and those of
+// each owned expert; the CTA turns these into the owned experts' first
+// packed rows (offsets) and each warp's first row per expert; a second pass
+// ranks the owned pairs in pair order (match groups per 32 pairs, in order)
+// and writes pair_row / row_token.  Integer counts only: deterministic, no
+// global atomics.  VEC: a lane reads four consecutive ids with one 16-byte
+// load (P % 4 == 0 and an aligned base); the second pass transposes each
+// 128-pair step through shared memory so that it walks them in pair order.
+template <bool VEC>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const int32_t* __restrict__ ids,
-                                                              int64_t P, int32_t topk, int32_t E,
+                                                              int64_t P, int32_t topk, int32_t E, int32_t epc,
                                                               int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ pair_row,
                                                               int32_t* __restrict__ row_token) {
     griddep_launch_dependents();
     griddep_wait();
-    constexpr int kWarps = kRouteThreads / 32;
-    __shared__ int s_lt[kWarps];
-    __shared__ int s_eq[kWarps];
-    const int e = blockIdx.x;
+    constexpr int kPer = VEC ? 4 : 1;      // ids per lane per step
+    constexpr int kStep = 32 * kPer;       // pairs per warp per step
+    constexpr int kU = 8;                  // steps whose loads are in flight together
+    __shared__ int s_cnt[kRouteWarps][kRouteMaxOwn + 1];   // per warp and owned expert
+    __shared__ int s_lt[kRouteWarps];
+    __shared__ int s_tot[kRouteMaxOwn];
+    __shared__ int s_ids[VEC ? kRouteWarps : 1][VEC ? kStep : 1];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // warp w owns the contiguous pairs [lo, hi) (a multiple of 32 long),
-    // read 32 at a time: one pass counts the pairs with id < e (expert e's
-    // first packed row) and those with id == e
-    const int64_t seg = ((P + kWarps - 1) / kWarps + 31) / 32 * 32;
+    const int e0 = blockIdx.x * epc;
+    const int ne = min(epc, E - e0);
+    for (int i = threadIdx.x; i < kRouteWarps * (kRouteMaxOwn + 1); i += kRouteThreads)
+        (&s_cnt[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t seg = ((P + kRouteWarps - 1) / kRouteWarps + kStep - 1) / kStep * kStep;
     const int64_t lo = min(P, seg * warp), hi = min(P, lo + seg);
-    int lt = 0, eq = 0;
-    // (unrolled: eight loads in flight per lane, not one L2 round trip per step)
-#pragma unroll 8
-    for (int64_t i0 = lo; i0 < hi; i0 += 32) {
-        const int64_t i = i0 + lane;
-        const int v = i < hi ? __ldg(ids + i) : -1;
-        lt += (i < hi && v < e) ? 1 : 0;
-        eq += __popc(__ballot_sync(0xFFFFFFFFu, v == e));
+    auto load = [&](int64_t i, int (&v)[kPer]) {   // -1: past the range
+        if constexpr (VEC) {
+            const int4 q = i < hi ? __ldg(reinterpret_cast<const int4*>(ids + i)) : make_int4(-1, -1, -1, -1);
+            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        } else {
+            v[0] = i < hi ? __ldg(ids + i) : -1;
+        }
+    };
+    // ---- pass 1: counts
+    int lt = 0;
+    for (int64_t c0 = lo; c0 < hi; c0 += kU * kStep) {
+        int v[kU][kPer];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) load(c0 + u * kStep + lane * kPer, v[u]);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t i = c0 + u * kStep + lane * kPer;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int id = v[u][j];
+                if (i < hi) {
+                    lt += id < e0 ? 1 : 0;
+                    if (id >= e0 && id < e0 + ne) atomicAdd(&s_cnt[warp][id - e0], 1);
+                }
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) lt += __shfl_xor_sync(0xFFFFFFFFu, lt, o);
-    if (lane == 0) {
-        s_lt[warp] = lt;
-        s_eq[warp] = eq;
+    if (lane == 0) s_lt[warp] = lt;
+    __syncthreads();
+    // per owned expert: the warps' counts become their exclusive prefix
+    if (threadIdx.x < ne) {
+        int run = 0;
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int c = s_cnt[w][threadIdx.x];
+            s_cnt[w][threadIdx.x] = run;
+            run += c;
+        }
+        s_tot[threadIdx.x] = run;
     }
     __syncthreads();
-    int base = 0, before = 0;
+    // first packed row of each owned expert; each warp's first row per expert
+    if (warp == 0) {
+        int below = 0;
+        for (int w = 0; w < kRouteWarps; ++w) below += s_lt[w];
+        const int tot = lane < ne ? s_tot[lane] : 0;
+        int inc = tot;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        base += s_lt[w];
-        if (w < warp) before += s_eq[w];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += n;
+        }
+        const int base = below + inc - tot;
+        if (lane < ne) {
+            offsets[e0 + lane] = base;
+            s_tot[lane] = base;
+        }
+        if (lane == 0 && e0 + ne == E) offsets[E] = static_cast<int32_t>(P);
     }
-    if (threadIdx.x == 0) {
-        offsets[e] = base;
-        if (e == E - 1) offsets[E] = static_cast<int32_t>(P);
-    }
-    // the pairs with id == e take packed rows base + rank, in pair order
-    int r = base + before;
-#pragma unroll 8
-    for (int64_t i0 = lo; i0 < hi; i0 += 32) {
-        const int64_t i = i0 + lane;
-        const bool hit = i < hi && __ldg(ids + i) == e;
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, hit);
-        if (hit) {
-            const int row = r + __popc(ball & ((1u << lane) - 1u));
+    __syncthreads();
+    if (lane < ne) s_cnt[warp][lane] += s_tot[lane];
+    __syncwarp();
+    // ---- pass 2: the owned pairs take their rows in pair order
+    const unsigned below_me = (1u << lane) - 1u;
+    auto place = [&](int64_t i, int id) {
+        const bool own = i < hi && id >= e0 && id < e0 + ne;
+        if (!__any_sync(0xFFFFFFFFu, own)) return;
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, own ? id : -1);
+        int row = 0;
+        if (own) {
+            row = s_cnt[warp][id - e0] + __popc(m & below_me);
             pair_row[i] = row;
             row_token[row] = static_cast<int32_t>(i / topk);
         }
-        r += __popc(ball);
+        __syncwarp();
+        if (own && (m >> lane) == 1u) s_cnt[warp][id - e0] = row + 1;   // the group's last lane
+        __syncwarp();
+    };
+    for (int64_t c0 = lo; c0 < hi; c0 += kU * kStep) {
+        int v[kU][kPer];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) load(c0 + u * kStep + lane * kPer, v[u]);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t s0 = c0 + u * kStep;
+            if constexpr (VEC) {
+                __syncwarp();   // the previous step's ids have been read
+                *reinterpret_cast<int4*>(&s_ids[warp][lane * 4]) = make_int4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) place(s0 + j * 32 + lane, s_ids[warp][j * 32 + lane]);
+            } else {
+                place(s0 + lane, v[u][0]);
+            }
+        }
     }
 }
 
@@ -221,8 +296,12 @@ extern "C" fp8_status fp8_moe_route(const int32_t* ids, int64_t T, int32_t topk,
     const int64_t P = T * topk;
     if (P > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
     if (P > 0 && (!ids || !pair_row || !row_token)) return FP8_ERR_INVALID_ARG;
-    route_kernel<<<E, kRouteThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        ids, P, topk, E, offsets, pair_row, row_token);
+    const bool vec = P % 4 == 0 && reinterpret_cast<uintptr_t>(ids) % 16 == 0;
+    auto kernel = vec ? route_kernel<true> : route_kernel<false>;
+    const int epc = (E + kRouteWarps - 1) / kRouteWarps;   // <= kRouteMaxOwn for E <= 1024
+    const int grid = (E + epc - 1) / epc;
+    kernel<<<grid, kRouteThreads, 0, static_cast<cudaStream_t>(stream)>>>(ids, P, topk, E, epc, offsets, pair_row,
+                                                                           row_token);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

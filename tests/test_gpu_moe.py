@@ -21,7 +21,10 @@ def fp8():
     return m
 
 
-@pytest.mark.parametrize("T,E,topk", [(4096, 256, 8), (300, 16, 4), (1, 8, 2), (37, 64, 6)])
+# T*topk % 4 == 0 takes the 16-byte-load path of the kernel (ragged warp
+# ranges included: 4093*8, 1000*2), the others the one-id-per-lane path
+@pytest.mark.parametrize("T,E,topk", [(4096, 256, 8), (4093, 256, 8), (1000, 8, 2), (300, 16, 4), (1, 8, 2),
+                                      (37, 64, 6)])
 def test_route_matches_oracle_exactly(fp8, T, E, topk):
     rt = syn.moe_routing(T=T, E=E, topk=topk, seed=T + E)
     off, pr, rtok = fp8.fp8_moe_route(dev_i32(rt.ids), E)
