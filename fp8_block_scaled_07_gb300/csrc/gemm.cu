@@ -232,6 +232,14 @@ struct DpIter {
         t += stride;
         return true;
     }
+    // the tile next() returns next, without advancing
+    __device__ bool peek(Seg& s) const {
+        if (t >= num_tiles) return false;
+        s.tile = t;
+        s.k0 = 0;
+        s.k1 = KB;
+        return true;
+    }
 };
 
 // Grouped: per-expert m-tiles (ceil(rows/128)) x N/BN n-tiles; tile index
@@ -775,52 +783,72 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
             }
             return true;
         };
+        // per-row a_s and per-block b_s, prefetched PF slabs ahead in registers
+        constexpr int PF = CPT >= 128 ? 4 : 8;   // prefetch distance (slabs)
+        float cs[PF], na[PF], nb[PF];
+        const float* ps = nullptr;
+        const float* qs = nullptr;
+        bool vec = false;
+        int sk1 = 0;
+        auto scale_rows = [&](const Tile& tg, const Seg& s) {
+            ps = p.a_s + static_cast<int64_t>(e < tg.p_valid ? tg.p_row0 + e : 0) * p.KB;
+            // (columns past N read the last block's scales; they are never stored)
+            qs = (V == kDense) ? p.b_s + static_cast<int64_t>(min((tg.q_row0 + cofs) / 128, p.NB - 1)) * p.KB
+                               : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + (tg.q_col0 + cofs) / 128) * p.KB;
+            // four slabs' scales per 16-byte load where the rows allow it
+            vec = p.vec_scales && (s.k0 % 4) == 0;
+            sk1 = s.k1;
+        };
+        auto load_next = [&](int base) {
+#pragma unroll
+            for (int i = 0; i < PF; i += 4) {
+                if (vec && base + i + 4 <= sk1) {
+                    const float4 va = __ldg(reinterpret_cast<const float4*>(ps + base + i));
+                    const float4 vb = __ldg(reinterpret_cast<const float4*>(qs + base + i));
+                    na[i] = va.x; na[i + 1] = va.y; na[i + 2] = va.z; na[i + 3] = va.w;
+                    nb[i] = vb.x; nb[i + 1] = vb.y; nb[i + 2] = vb.z; nb[i + 3] = vb.w;
+                } else {
+#pragma unroll
+                    for (int j = i; j < i + 4; ++j) {
+                        const int kb = base + j;
+                        na[j] = kb < sk1 ? __ldg(ps + kb) : 0.0f;
+                        nb[j] = kb < sk1 ? __ldg(qs + kb) : 0.0f;
+                    }
+                }
+            }
+        };
+        bool ahead = false;   // na/nb already hold this tile's first PF scales
         while (ok && it.next(sg)) {
             const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
             float acc[CPT];
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
-            {
-                // per-row a_s and per-block b_s, prefetched PF slabs ahead in registers
-                const float* ps = p.a_s + static_cast<int64_t>(e < tg.p_valid ? tg.p_row0 + e : 0) * p.KB;
-                // (columns past N read the last block's scales; they are never stored)
-                const float* qs = (V == kDense)
-                                      ? p.b_s + static_cast<int64_t>(min((tg.q_row0 + cofs) / 128, p.NB - 1)) * p.KB
-                                      : p.b_s + (static_cast<int64_t>(tg.group) * p.NB + (tg.q_col0 + cofs) / 128) * p.KB;
-                constexpr int PF = CPT >= 128 ? 4 : 8;   // prefetch distance (slabs)
-                float cs[PF], na[PF], nb[PF];
-                // four slabs' scales per 16-byte load where the rows allow it
-                const bool vec = p.vec_scales && (sg.k0 % 4) == 0;
-                auto load_next = [&](int base) {
-#pragma unroll
-                    for (int i = 0; i < PF; i += 4) {
-                        if (vec && base + i + 4 <= sg.k1) {
-                            const float4 va = __ldg(reinterpret_cast<const float4*>(ps + base + i));
-                            const float4 vb = __ldg(reinterpret_cast<const float4*>(qs + base + i));
-                            na[i] = va.x; na[i + 1] = va.y; na[i + 2] = va.z; na[i + 3] = va.w;
-                            nb[i] = vb.x; nb[i + 1] = vb.y; nb[i + 2] = vb.z; nb[i + 3] = vb.w;
-                        } else {
-#pragma unroll
-                            for (int j = i; j < i + 4; ++j) {
-                                const int kb = base + j;
-                                na[j] = kb < sg.k1 ? __ldg(ps + kb) : 0.0f;
-                                nb[j] = kb < sg.k1 ? __ldg(qs + kb) : 0.0f;
-                            }
-                        }
-                    }
-                };
+            if (!ahead) {
+                scale_rows(tg, sg);
                 load_next(sg.k0);
+            }
+#pragma unroll
+            for (int i = 0; i < PF; ++i) cs[i] = na[i] * nb[i];
+            load_next(sg.k0 + PF);
+            for (int kc = sg.k0; kc < sg.k1 && ok; kc += PF) {
+#pragma unroll
+                for (int i = 0; i < PF; ++i) {
+                    if (ok && kc + i < sg.k1) ok = take_slab(acc, nullptr, cs[i]);
+                }
 #pragma unroll
                 for (int i = 0; i < PF; ++i) cs[i] = na[i] * nb[i];
-                load_next(sg.k0 + PF);
-                for (int kc = sg.k0; kc < sg.k1 && ok; kc += PF) {
-#pragma unroll
-                    for (int i = 0; i < PF; ++i) {
-                        if (ok && kc + i < sg.k1) ok = take_slab(acc, nullptr, cs[i]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < PF; ++i) cs[i] = na[i] * nb[i];
-                    load_next(kc + 2 * PF);
+                load_next(kc + 2 * PF);
+            }
+            ahead = false;
+            // dense whole-tile schedule: fetch the next tile's first scales
+            // now, so that their latency hides behind this tile's output
+            // store (the grouped kernel measured slower with it)
+            if constexpr (C::kSplitRegs && V == kDense) {
+                Seg nx;
+                if (ok && it.peek(nx)) {
+                    scale_rows(tile_geom<BN, V>(p, nx.tile, s_prefix), nx);
+                    load_next(nx.k0);
+                    ahead = true;
                 }
             }
             if (!ok) break;

@@ -192,6 +192,9 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint4* __restr
     const int64_t KB = K / kBlock, nblocks = T * KB;
     const int64_t hw = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 2 + half;
     const int64_t nhw = ((static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) * 2;
+    // the two half-warps may run different numbers of blocks (an odd block
+    // count), so each reduces over its own 16 lanes only
+    const unsigned hmask = 0xFFFFu << (half * 16);
     for (int64_t blk = hw; blk < nblocks; blk += nhw) {
         const int64_t t = blk / KB, kb = blk - t * KB;
         float f[8];
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(256) quant_scatter_kernel(const uint4* __restr
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, o));
         const float sc = block_scale(amax, UE8M0);
         const uint2 q = quant8<UE8M0>(f, sc);
         for (int j = 0; j < topk; ++j) {

@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
     constexpr int U = 2;
-    for (int64_t b0 = warp * (2 * U); b0 < nblocks; b0 += nwarps * (2 * U)) {
-        uint4 v1[U], v3[U];
+    // the next iteration's loads are issued before this one's arithmetic
+    auto load = [&](int64_t b0, uint4 (&v1)[U], uint4 (&v3)[U]) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t blk = b0 + 2 * u + half;
@@ -192,6 +192,17 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(
                 v3[u] = make_uint4(0, 0, 0, 0);
             }
         }
+    };
+    uint4 n1[U], n3[U];
+    load(warp * (2 * U), n1, n3);
+    for (int64_t b0 = warp * (2 * U); b0 < nblocks; b0 += nwarps * (2 * U)) {
+        uint4 v1[U], v3[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            v1[u] = n1[u];
+            v3[u] = n3[u];
+        }
+        load(b0 + nwarps * (2 * U), n1, n3);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t blk = b0 + 2 * u + half;

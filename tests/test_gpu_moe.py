@@ -34,6 +34,23 @@ def test_route_matches_oracle_exactly(fp8, T, E, topk):
     assert np.array_equal(rtok.cpu().numpy(), o_rtok)
 
 
+# odd block counts (37 x 3 blocks), topk above 16 (rows read directly past
+# the first 16), and the model's shape; both scale formats
+@pytest.mark.parametrize("T,K,topk,E", [(37, 384, 6, 16), (5, 128, 20, 32), (300, 7168, 8, 256)])
+@pytest.mark.parametrize("ue8m0", [False, True])
+def test_quant_scatter_equals_oracle_act_quant_then_gather(fp8, T, K, topk, E, ue8m0):
+    rt = syn.moe_routing(T=T, E=E, topk=topk, seed=T + K)
+    x = syn.normal_bf16(np.random.default_rng(T), (T, K))
+    _, pr, _ = fp8.fp8_moe_route(dev_i32(rt.ids), E)
+    aq, as_ = fp8.fp8_moe_quant_scatter(dev_bf16(x), pr, fp8.FP8_SCALE_UE8M0 if ue8m0 else fp8.FP8_SCALE_FP32)
+    fp8.fp8_device_status()
+    # the oracle: act_quant of every token row, then the packed rows in order
+    xq, xs = oracle.act_quant(x, ue8m0=ue8m0)
+    _, _, rtok = oracle.moe_route(rt.ids, E)
+    assert np.array_equal(host_bits(aq), xq[rtok])
+    assert np.array_equal(host_f32(as_).view(np.uint32), xs[rtok].view(np.uint32))
+
+
 def test_gather_rows(fp8):
     rt = syn.moe_routing(T=300, E=16, topk=4, seed=2)
     x = syn.normal_bf16(np.random.default_rng(1), (300, 512))
