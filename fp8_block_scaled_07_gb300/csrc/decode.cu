@@ -73,14 +73,17 @@ constexpr int kDecStages = 3;   // pipeline stages (one 128-K slab each)
 // long weight streams, and room left for most of the next launch's CTAs to
 // be resident and waiting when this one ends (measured on GB300, decode
 // step at M = 16 / the wo layer alone, back to back: 50% 41.4 / 28.2 us,
-// 60% 41.4 / 28.2, 66% 42.7 / 24.6, 75% 40.0 / 22.7, 100% 50.4 / 29.7);
-// 32- and 64-token tiles (two per SM): all, their streams need the bytes in
-// flight (M = 64: 74.1 us against 85.4 us at half).
+// 60% 41.4 / 28.2, 66% 42.7 / 24.6, 75% 40.0 / 22.7, 100% 50.4 / 29.7).
+// 32- and 64-token tiles (two per SM): three quarters as well.  With all
+// slots, wo's clusters of 5 could not all be placed while the previous
+// layer's CTAs were still resident, and the last ones ran as a second wave
+// (decode step at M = 32 / 48 / 64: all 56.5 / 82.2 / 86.9 us, 75% 49.8 /
+// 75.7 / 78.8, 70% 52.2 / 86.8 / 91.1, half 85.4 at M = 64).
 #ifndef FP8BS_DEC_FILL16
 #define FP8BS_DEC_FILL16 75
 #endif
 #ifndef FP8BS_DEC_FILL
-#define FP8BS_DEC_FILL 100
+#define FP8BS_DEC_FILL 75
 #endif
 
 template <int BN, int S>
