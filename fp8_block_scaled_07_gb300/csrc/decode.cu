@@ -18,11 +18,12 @@
 //     every row of its partial into the shared memory of the CTA owning that
 //     row (st.async, counted as transaction bytes on the owner's barrier) --
 //     and the owner sums them in rank order (deterministic).
-//   * One 128-K slab per pipeline stage, three stages, so 2-3 CTAs fit on an
-//     SM, and a 16-token launch takes about three quarters of the CTA slots:
-//     with programmatic dependent launch most of the next launch's CTAs are
-//     resident and set up while this one runs, and they pass
-//     griddepcontrol.wait together.
+//   * One 128-K slab per pipeline stage: three stages for 16-token tiles (3
+//     CTAs per SM), four for 32 (2 per SM), four or three for 64 (1 or 2 per
+//     SM, by the layer's tile count); a launch takes about three quarters of
+//     the CTA slots: with programmatic dependent launch most of the next
+//     launch's CTAs are resident and set up while this one runs, and they
+//     pass griddepcontrol.wait together.
 //   * Four "activation" warps feed the token side of each slab: they load
 //     their values from global memory one slab ahead, quantise them (fused;
 //     the library's act_quant routine) or take the e4m3 codes as they are,
@@ -67,7 +68,15 @@ constexpr int kDecMaxCluster = 16;
 #define FP8BS_DEC_EVICT_FIRST 1   // weight loads marked evict-first in L2 (each byte is read once)
 #endif
 
-constexpr int kDecStages = 3;   // pipeline stages (one 128-K slab each)
+// Pipeline stages (one 128-K slab each).  16-token tiles: 3 (three CTAs per
+// SM).  32-token tiles: 4 (still two per SM; decode step at M = 32 49.9 ->
+// 48.8 us against 3).  64-token tiles: 4, one CTA per SM, when the layer's
+// tiles fit one wave of that, else 3 (two per SM): at M = 64 wo took 37.4
+// against 46.5 us and wq_a 12.8 against 15.8, but wq_b's 192 tiles 20.5
+// against 18.5 us in two waves.
+constexpr int kDecStages = 3;
+constexpr int kS32 = 4;
+constexpr int kS64Deep = 4;
 // Percent of the device's CTA slots one launch may take.  16-token tiles
 // (three CTAs per SM): three quarters -- enough bytes in flight for the
 // long weight streams, and room left for most of the next launch's CTAs to
@@ -550,16 +559,34 @@ void plan_split(DecPlan& pl, int KB, long long budget, int cmax) {
     pl.grid = pl.tiles * best_c;
 }
 
-DecPlan decode_plan(int64_t M, int64_t N, int64_t K, int sms, int cmax) {
+// (the fused and plain kernels of a tile width need the same resources, so
+// one cluster-size query serves both and their plans agree)
+DecPlan decode_plan(int64_t M, int64_t N, int64_t K, int sms, int dev) {
     DecPlan pl{};
     pl.bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     pl.tiles = static_cast<int>((N + 127) / 128);
-    pl.stages = kDecStages;
     const int KB = static_cast<int>(K / kBlock);
-    const int per_sm = pl.bn == 16 ? Dec<16, kDecStages>::kMinBlocks
-                                   : (pl.bn == 32 ? Dec<32, kDecStages>::kMinBlocks : Dec<64, kDecStages>::kMinBlocks);
     const int fill = pl.bn == 16 ? FP8BS_DEC_FILL16 : FP8BS_DEC_FILL;
-    plan_split(pl, KB, std::max<long long>(1, static_cast<long long>(sms) * per_sm * fill / 100), cmax);
+    auto budget = [&](int per_sm) { return std::max<long long>(1, static_cast<long long>(sms) * per_sm * fill / 100); };
+    int per_sm = 1, cmax = 1;
+    if (pl.bn == 16) {
+        pl.stages = kDecStages;
+        per_sm = Dec<16, kDecStages>::kMinBlocks;
+        cmax = max_cluster<16, false, kDecStages>(dev);
+    } else if (pl.bn == 32) {
+        pl.stages = kS32;
+        per_sm = Dec<32, kS32>::kMinBlocks;
+        cmax = max_cluster<32, false, kS32>(dev);
+    } else if (pl.tiles <= budget(Dec<64, kS64Deep>::kMinBlocks)) {
+        pl.stages = kS64Deep;
+        per_sm = Dec<64, kS64Deep>::kMinBlocks;
+        cmax = max_cluster<64, false, kS64Deep>(dev);
+    } else {
+        pl.stages = kDecStages;
+        per_sm = Dec<64, kDecStages>::kMinBlocks;
+        cmax = max_cluster<64, false, kDecStages>(dev);
+    }
+    plan_split(pl, KB, budget(per_sm), cmax);
     return pl;
 }
 
@@ -570,14 +597,6 @@ cudaError_t launch_decode(const CUtensorMap& tw, const CUtensorMap& tx, const De
     if (!configure<BN, FUSED, S>(dev)) return cudaErrorInvalidValue;
     return launch_pdl_cluster(decode_kernel<BN, FUSED, S>, dim3(grid), dim3(kDecThreads), Dec<BN, S>::kSmemBytes,
                               st, cluster, tw, tx, prm);
-}
-
-// (the fused and plain kernels of a tile width need the same resources, so
-// one query serves both and their plans agree)
-int plan_cmax(int bn, int dev) {
-    if (bn == 16) return max_cluster<16, false, kDecStages>(dev);
-    if (bn == 32) return max_cluster<32, false, kDecStages>(dev);
-    return max_cluster<64, false, kDecStages>(dev);
 }
 
 #ifdef FP8BS_TRACE_ENABLED
@@ -596,8 +615,7 @@ fp8_status decode_gemm(const void* x, const void* xq, const float* a_s, const vo
     if (dev < 0) return FP8_ERR_CUDA;
     const bool fused = x != nullptr;
     if (fused && M > kDecodeFusedMaxM) return FP8_ERR_UNSUPPORTED;
-    const int bn0 = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-    const DecPlan pl = decode_plan(M, N, K, device_sm_count(), plan_cmax(bn0, dev));
+    const DecPlan pl = decode_plan(M, N, K, device_sm_count(), dev);
     if (static_cast<long long>(pl.tiles) * pl.c > (1LL << 31) - 1) return FP8_ERR_UNSUPPORTED;
     DecParams prm{};
     prm.xq = static_cast<const uint8_t*>(xq);
@@ -626,7 +644,9 @@ fp8_status decode_gemm(const void* x, const void* xq, const float* a_s, const vo
         e = fused ? launch_decode<16, true, kDecStages>(tw, tx, prm, pl.grid, cl, st)
                   : launch_decode<16, false, kDecStages>(tw, tx, prm, pl.grid, cl, st);
     else if (pl.bn == 32)
-        e = launch_decode<32, false, kDecStages>(tw, tx, prm, pl.grid, cl, st);
+        e = launch_decode<32, false, kS32>(tw, tx, prm, pl.grid, cl, st);
+    else if (pl.stages == kS64Deep)
+        e = launch_decode<64, false, kS64Deep>(tw, tx, prm, pl.grid, cl, st);
     else
         e = launch_decode<64, false, kDecStages>(tw, tx, prm, pl.grid, cl, st);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
