@@ -136,7 +136,11 @@ template <int BN, int V, bool SW = false>
 struct Cfg {
     static constexpr int kQTileBytes = BN * kBlock;
     static constexpr int kStageBytes = kPTileBytes + kQTileBytes;
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    // the expert body of a 128x256 tile runs on warps 2-3 ("gate warps"),
+    // from the tile's bf16 h left in shared memory by the epilogue warps
+    static constexpr bool kGate = SW && BN == 256;
+    static constexpr int kHBytes = 128 * 256 * 2;
+    static constexpr int kStages = BN == 256 ? (kGate ? 3 : 4) : 6;
     // 128x256 tiles: 8 epilogue warps, two per TMEM lane quarter, each owning
     // 128 of the 256 columns; their warpgroups take registers from warps 0-3
     static constexpr int kEpiWarps = BN == 256 ? 8 : 4;
@@ -159,9 +163,10 @@ struct Cfg {
     // per epilogue warp a staging box (kStgRows rows x 64 bf16, 128-byte
     // swizzle) through which output tiles leave by TMA stores; 32 rows dense,
     // 16 grouped (whose expert-tile prefix takes the room)
+    // (the gate kernels use the room for the h tile instead)
     static constexpr bool kTmaStore = true;
     static constexpr int kStgRows = V == kGrouped ? 16 : 32;
-    static constexpr int kStgBytes = kEpiWarps * kStgRows * 128;
+    static constexpr int kStgBytes = kGate ? kHBytes : kEpiWarps * kStgRows * 128;
     static constexpr int kSmemBytes =
         1024 /*align slack*/ + kStages * kStageBytes + kStgBytes + kBarBytes + kExtraBytes;
 };
@@ -275,6 +280,10 @@ __device__ __forceinline__ Tile tile_geom(const Params& p, int t, const int* s_p
     return g;
 }
 
+__device__ __noinline__ bool gate_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait(bar, parity, abort_flag);
+}
+
 __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
     *abort_flag = 1;
     atomicExch(&g_gemm_status, static_cast<int>(FP8_ERR_TIMEOUT));
@@ -373,106 +382,6 @@ __device__ __forceinline__ int store_tile_tma(const CUtensorMap* tm_c, uint8_t* 
     return 32;
 }
 
-// The expert body fused into the epilogue of a 128x256 tile of the w1|w3
-// product ("Behavior traces", bullet "MoE trace": each expert computes
-// w2(silu(w1 x) * w3 x); source tour, "FP8 with per-block scales": the
-// input of w2 is quantised per 128 block).  The weights are interleaved so
-// that tile columns 0-127 are h1 = x w1^T and 128-255 are h3 = x w3^T of the
-// same 128-wide block of the intermediate dimension.  The two epilogue warps
-// of a TMEM lane quarter (half 0: h1, half 1: h3, the same 32 rows) swap
-// halves through their staging boxes (ROWS rows at a time): half 0 then
-// makes g for columns 0-63, half 1 for columns 64-127, with the library's
-// silu*mul routine on the bf16-rounded h values (what the GEMM would have
-// stored); the row's block max is combined through the boxes too, and each
-// warp quantises its 64 values with act_quant's routine and stores their
-// codes, half 0 also the row's scale.  Bit-identical to storing h in bf16
-// and running the standalone silu*mul+act_quant on it.
-template <int ROWS>
-__device__ __forceinline__ void swiglu_quant_epilogue(const Params& p, uint8_t* my_box, const uint8_t* peer_box,
-                                                      int half, int lane, int q, bool row_valid, int64_t out_row,
-                                                      int iblk, const float (&acc)[128]) {
-    // bf16 pairs of the 64 values this warp keeps (half 0: h1[0:64], half 1:
-    // h3[64:128]) and of the 64 it gives away (h1[64:128], h3[0:64]); the
-    // accumulators are dead after this loop (constant indices in both
-    // branches keep them in registers)
-    uint32_t keep[32], give[32], recv[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[64 + 2 * j], acc[64 + 2 * j + 1]);
-        const uint32_t ulo = *reinterpret_cast<const uint32_t*>(&lo), uhi = *reinterpret_cast<const uint32_t*>(&hi);
-        keep[j] = half == 0 ? ulo : uhi;
-        give[j] = half == 0 ? uhi : ulo;
-    }
-#pragma unroll
-    for (int r0 = 0; r0 < 32; r0 += ROWS) {
-        const bool mine = lane >= r0 && lane < r0 + ROWS;
-        const int row = lane - r0;
-        if (mine) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(my_box + row * 128 + ((c ^ (row & 7)) * 16)) =
-                    make_uint4(give[4 * c], give[4 * c + 1], give[4 * c + 2], give[4 * c + 3]);
-        }
-        named_bar_sync(1 + q, 64);
-        if (mine) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = *reinterpret_cast<const uint4*>(peer_box + row * 128 + ((c ^ (row & 7)) * 16));
-                recv[4 * c] = v.x;
-                recv[4 * c + 1] = v.y;
-                recv[4 * c + 2] = v.z;
-                recv[4 * c + 3] = v.w;
-            }
-        }
-        named_bar_sync(1 + q, 64);   // both read before the boxes are written again
-    }
-    // g of this warp's 64 columns, packed bf16 pairs
-    uint32_t g[32];
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const uint32_t u1 = half == 0 ? keep[j] : recv[j];   // h1 pair
-        const uint32_t u3 = half == 0 ? recv[j] : keep[j];   // h3 pair
-        g[j] = silu_mul_bf16x2(__uint_as_float(u1 << 16), __uint_as_float(u1 & 0xFFFF0000u),
-                               __uint_as_float(u3 << 16), __uint_as_float(u3 & 0xFFFF0000u));
-        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(g[j] << 16)), fabsf(__uint_as_float(g[j] & 0xFFFF0000u))));
-    }
-    // the row's block max over both halves
-    float peer_amax = 0.0f;
-#pragma unroll
-    for (int r0 = 0; r0 < 32; r0 += ROWS) {
-        const bool mine = lane >= r0 && lane < r0 + ROWS;
-        const int row = lane - r0;
-        if (mine) *reinterpret_cast<float*>(my_box + row * 128) = amax;
-        named_bar_sync(1 + q, 64);
-        if (mine) peer_amax = *reinterpret_cast<const float*>(peer_box + row * 128);
-        named_bar_sync(1 + q, 64);
-    }
-    amax = fmaxf(amax, peer_amax);
-    const float sc = block_scale(amax, p.ue8m0 != 0);
-    if (!row_valid) return;
-    const int I = p.N / 2;
-    uint4* dst = reinterpret_cast<uint4*>(p.gq + out_row * I + iblk * 128 + half * 64);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint2 qv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float f[8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t w = g[8 * c + 4 * h + u];
-                f[2 * u] = __uint_as_float(w << 16);
-                f[2 * u + 1] = __uint_as_float(w & 0xFFFF0000u);
-            }
-            qv[h] = p.ue8m0 ? quant8<true>(f, sc) : quant8<false>(f, sc);
-        }
-        dst[c] = make_uint4(qv[0].x, qv[0].y, qv[1].x, qv[1].y);
-    }
-    if (half == 0) p.gs[out_row * (I / 128) + iblk] = sc;
-}
-
 // Exclusive prefix over experts of their tile counts (m-tiles x tq), by the
 // whole block: each thread takes up to 4 experts, then a block-wide scan.
 // G <= kMaxGroups and NT >= 256, so 4 experts per thread always suffice.
@@ -566,8 +475,11 @@ __device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& phase, const v
     return ok;
 }
 
-// SW: the expert body fused into the epilogue (a kernel of its own, so
-// that the plain kernels' register allocation does not carry it)
+// SW: the expert body fused into the w1|w3 product (a kernel of its own,
+// so that the plain kernels' register allocation does not carry it): the
+// epilogue warps leave each finished 128x256 tile in shared memory as bf16
+// and go on to the next tile; warps 2-3, idle in the plain kernels, turn it
+// into g's codes and scales meanwhile.
 template <int BN, int V, bool SW>
 __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::kMinBlocks))
     gemm_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
@@ -587,7 +499,9 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
     uint64_t* tempty = bars + 2 * S + 2;   // 2
     uint64_t* mma_done = bars + 2 * S + 4; // 1
     uint64_t* epi_bar = bars + 2 * S + 5;  // epilogue-group barrier
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+    uint64_t* h_full = bars + 2 * S + 6;   // gate kernels: the h tile is in shared memory
+    uint64_t* h_empty = bars + 2 * S + 7;  // gate kernels: the gate warps have read it
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* ticket_box = reinterpret_cast<volatile int*>(tmem_holder + 2);
     int* s_prefix = reinterpret_cast<int*>(smem + S * C::kStageBytes + C::kStgBytes + C::kBarBytes);
@@ -615,6 +529,8 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
         }
         mbar_init(mma_done, 1);
         mbar_init(epi_bar, 32 * C::kEpiWarps);
+        mbar_init(h_full, 32 * C::kEpiWarps);   // one arrival per epilogue thread
+        mbar_init(h_empty, 64);                 // one arrival per gate thread
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -741,6 +657,76 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
             const volatile int never = 0;
             if (!mbar_wait(mma_done, 0, &never)) set_abort(abort_flag);
         }
+    } else if constexpr (C::kGate) {
+        // ---------------------------------------------------------- gate warps (2-3)
+        // The expert body of each finished tile, while the epilogue warps
+        // promote the next one: g = bf16(bf16(silu(h1)) * h3) from the
+        // tile's bf16 h (h1 in columns 0-127, h3 in 128-255 of the same
+        // 128-wide block of the intermediate dimension), then act_quant of
+        // each row's 128 values.  Two rows per thread; the library's
+        // silu*mul and quantisation routines, so the codes and scales equal
+        // those of the unfused chain bit for bit.
+        griddep_wait();   // before the first store of g
+        const int gt = static_cast<int>(threadIdx.x) - 64;   // 0..63
+        const int I = p.N / 2;
+        uint32_t hn = 0;
+        while (it.next(sg)) {
+            const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
+            if (!mbar_wait(h_full, hn & 1, abort_flag)) {
+                set_abort(abort_flag);
+                break;
+            }
+            const int iblk = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) / 256;
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                const int r = gt + 64 * pass;
+                uint8_t* hrow = sStg + r * 512;
+                // g over h1's place in the row (the row is this thread's alone)
+                float amax = 0.0f;
+#pragma unroll 4
+                for (int c = 0; c < 16; ++c) {
+                    // chunk c: eight columns of h1 (chunk c) and of h3 (chunk 16 + c)
+                    uint4* pa = reinterpret_cast<uint4*>(hrow + ((c ^ (r & 7)) * 16));
+                    const uint4 a = *pa;
+                    const uint4 b = *reinterpret_cast<const uint4*>(hrow + (((16 + c) ^ (r & 7)) * 16));
+                    const uint32_t u1[4] = {a.x, a.y, a.z, a.w}, u3[4] = {b.x, b.y, b.z, b.w};
+                    uint32_t g[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        g[i] = silu_mul_bf16x2(__uint_as_float(u1[i] << 16), __uint_as_float(u1[i] & 0xFFFF0000u),
+                                               __uint_as_float(u3[i] << 16), __uint_as_float(u3[i] & 0xFFFF0000u));
+                        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(g[i] << 16)),
+                                                 fabsf(__uint_as_float(g[i] & 0xFFFF0000u))));
+                    }
+                    *pa = make_uint4(g[0], g[1], g[2], g[3]);
+                }
+                const float sc = block_scale(amax, p.ue8m0 != 0);
+                if (r < tg.p_valid) {
+                    const int64_t row = static_cast<int64_t>(tg.p_row0) + r;
+                    uint4* dst = reinterpret_cast<uint4*>(p.gq + row * I + iblk * 128);
+#pragma unroll 2
+                    for (int c = 0; c < 8; ++c) {   // 16 codes per store, from g chunks 2c and 2c + 1
+                        uint2 qv[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(hrow + (((2 * c + h) ^ (r & 7)) * 16));
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                            float f[8];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                f[2 * u] = __uint_as_float(w[u] << 16);
+                                f[2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u);
+                            }
+                            qv[h] = p.ue8m0 ? quant8<true>(f, sc) : quant8<false>(f, sc);
+                        }
+                        dst[c] = make_uint4(qv[0].x, qv[0].y, qv[1].x, qv[1].y);
+                    }
+                    p.gs[row * (I / 128) + iblk] = sc;
+                }
+            }
+            mbar_arrive(h_empty);   // this thread's rows are done with
+            ++hn;
+        }
     }
     } else {
         if constexpr (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
@@ -818,6 +804,7 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
             }
         };
         bool ahead = false;   // na/nb already hold this tile's first PF scales
+        uint32_t hn = 0;      // gate kernels: tiles handed to the gate warps
         while (ok && it.next(sg)) {
             const Tile tg = tile_geom<BN, V>(p, sg.tile, s_prefix);
             float acc[CPT];
@@ -855,17 +842,39 @@ __global__ void __launch_bounds__((Cfg<BN, V, SW>::kThreads), (Cfg<BN, V, SW>::k
             if (e == 0) FP8BS_TRACE(5);
             if (sg.k0 == 0 && sg.k1 == p.KB) {
                 FP8BS_TIC(t5_);
-                if constexpr (SW && BN == 256) {
-                    {
-                        const int half = (warp - kEpiWarp0) >> 2;
-                        uint8_t* my_box = sStg + (warp - kEpiWarp0) * (C::kStgRows * 128);
-                        const uint8_t* peer_box = sStg + ((warp - kEpiWarp0) ^ 4) * (C::kStgRows * 128);
-                        const int iblk = ((V == kGrouped) ? tg.q_col0 : tg.q_row0) / 256;
-                        swiglu_quant_epilogue<C::kStgRows>(p, my_box, peer_box, half, lane, q, e < tg.p_valid,
-                                                           static_cast<int64_t>(tg.p_row0) + e, iblk, acc);
-                        FP8BS_TOC(w_store, t5_);
-                        continue;
+                if constexpr (C::kGate) {
+                    // hand the tile to the gate warps: row e's 128 columns of
+                    // h (this thread's half: h1 or h3) as bf16, in 16-byte
+                    // chunks whose order within each group of eight is
+                    // swizzled by the row (conflict-free for both sides);
+                    // first wait until the gate warps have read the last tile
+                    // (the usual case, the gate warps long done, costs one
+                    // try_wait; the bounded wait sits out of line so that
+                    // its state does not compete with the accumulators)
+                    bool hfree = mbar_try_wait(smem_u32(h_empty), (hn & 1) ^ 1);
+                    if (!warp_all(hfree)) hfree = gate_wait_slow(h_empty, (hn & 1) ^ 1, abort_flag);
+                    if (!warp_all(hfree)) {
+                        set_abort(abort_flag);
+                        ok = false;
+                        break;
                     }
+                    const int half = (warp - kEpiWarp0) >> 2;
+                    uint8_t* hrow = sStg + e * 512;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[8 * c + 2 * i], acc[8 * c + 2 * i + 1]);
+                            w[i] = *reinterpret_cast<const uint32_t*>(&b);
+                        }
+                        *reinterpret_cast<uint4*>(hrow + (((half * 16 + c) ^ (e & 7)) * 16)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    mbar_arrive(h_full);
+                    ++hn;
+                    FP8BS_TOC(w_store, t5_);
+                    continue;
                 }
                 if constexpr (C::kTmaStore) {
                     if (p.tma_store) {

@@ -199,7 +199,8 @@ fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const void* w13, con
  * Expert g owns the packed rows [offsets[g], offsets[g+1]) of a [R_max, K]
  * e4m3 (scales a_s [R_max, K/128]); its w13 ([G, 2I, K], interleaved as for
  * fp8_gemm_swiglu; scales [G, 2I/128, K/128]) makes h1, h3, and the gate and
- * act_quant run in the epilogue -> g_q [R_max, I] e4m3, g_s [R_max, I/128]
+ * act_quant run on chip on each finished tile -> g_q [R_max, I] e4m3,
+ * g_s [R_max, I/128]
  * in packed row order (rows past offsets[G] are not written).  offsets:
  * int32 [G+1] in device memory.  The same bytes as fp8_grouped_gemm (bf16
  * out) followed by fp8_silu_mul_quant.  Requires I % 128 == 0,
