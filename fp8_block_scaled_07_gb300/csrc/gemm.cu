@@ -1968,6 +1968,7 @@ extern "C" fp8_status fp8_gemm_swiglu(const void* a, const float* a_s, const voi
     prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
     prm.gq = static_cast<uint8_t*>(g_q);
     prm.gs = g_s;
+    prm.debug_skip = g_debug_skip_next.exchange(0);
 #ifdef FP8BS_TRACE_ENABLED
     prm.trace_slot = g_trace_next++ & 3;
 #endif
@@ -2004,6 +2005,7 @@ extern "C" fp8_status fp8_moe_expert_up(const void* a, const float* a_s, const v
     prm.ue8m0 = scale_fmt == FP8_SCALE_UE8M0 ? 1 : 0;
     prm.gq = static_cast<uint8_t*>(g_q);
     prm.gs = g_s;
+    prm.debug_skip = g_debug_skip_next.exchange(0);
 #ifdef FP8BS_TRACE_ENABLED
     prm.trace_slot = g_trace_next++ & 3;
 #endif

@@ -54,3 +54,34 @@ def test_withheld_handoff_times_out_and_the_stream_recovers(fp8):
     assert _status(fp8) == 0
     ref, mag = oracle.gemm(a, a_s, b, b_s)
     check_gemm(ref, mag, host_f32(cf), host_bits(cb), "after the timeout")
+
+
+def test_fused_gate_times_out_and_the_stream_recovers(fp8):
+    # the w1|w3 kernel with the gate on warps 2-3: the epilogue's wait runs
+    # out, the tile never reaches the gate warps, whose own bounded wait
+    # then ends on the abort; the next call equals the unfused chain
+    # 128 x 256 tiles (h1 | h3) of one 128-K slab; M large enough that the
+    # unfused fp8_gemm runs the same whole-tile kernel (same fp32 order)
+    M, I, K = 300, 128, 128
+    a = syn.random_e4m3_codes((M, K), 211)
+    w13 = syn.random_e4m3_codes((2 * I, K), 212)   # one 128-row block each of w1 and w3
+    a_s = syn.random_scales((M, K // 128), 213)
+    w_s = syn.random_scales((2 * I // 128, K // 128), 214)
+    args = (dev_e4m3(a), dev_f32(a_s), dev_e4m3(w13), dev_f32(w_s))
+    torch.cuda.synchronize()
+    assert _status(fp8) == 0
+    assert fp8.lib.fp8_debug_set_wait_limit(2_000_000) == 0
+    try:
+        fp8.lib.fp8_debug_skip_one_arrive()
+        fp8.fp8_gemm_swiglu(*args)
+        assert _status(fp8) == FP8_ERR_TIMEOUT
+        assert _status(fp8) == 0
+    finally:
+        torch.cuda.synchronize()
+        assert fp8.lib.fp8_debug_set_wait_limit(0) == 0
+    gq, gs = fp8.fp8_gemm_swiglu(*args)
+    h, _ = fp8.fp8_gemm(*args, out_bf16=True)
+    yq, ys, _ = fp8.fp8_silu_mul_quant(h, h[:, I:], 2 * I, M, I)
+    assert _status(fp8) == 0
+    assert torch.equal(gq.view(torch.uint8), yq.view(torch.uint8))
+    assert torch.equal(gs.view(torch.int32), ys.view(torch.int32))
