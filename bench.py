@@ -61,6 +61,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ------------------------------------------------------------------ accounting
+def workload_config(world):
+    """The headline workload, the same in both arms' JSON lines."""
+    return {"workload": "decode linears wq_a 7168->1536, wq_b 1536->24576, wo 16384->7168; "
+                        "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear: one kernel per "
+                        "layer, the quantisation inside the GEMM)",
+            "global_batch": M_DECODE * world, "parallelism": f"replicas x{world}"}
+
+
 def act_quant_bytes(M, K):
     return M * K * 2 + M * K + 4 * M * (K // 128)
 
@@ -695,8 +703,7 @@ def run_reference(args, rank, world):
             "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode linears wq_a/wq_b/wo, M=16 tokens, e4m3 weights 128x128 fp32 scales",
-                       "global_batch": M_DECODE, "parallelism": "replicas"},
+            "config": workload_config(args.gpus),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": omp_threads(), "kind": "oracle",
                              "sample": f"per step: act_quant of all 3 inputs + GEMM over 1/{frac} of each "
                                        f"layer's output features (bytes scaled to the sample)"},
@@ -1018,12 +1025,9 @@ def main():
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out", "data": "synthetic",
-        "config": {"workload": "decode linears wq_a 7168->1536, wq_b 1536->24576, wo 16384->7168; "
-                               "M=16 tokens; act_quant + fp8_gemm per layer (fp8_linear: one kernel per "
-                               "layer, the quantisation inside the GEMM)",
-                   "global_batch": M * world, "parallelism": f"replicas x{world}",
-                   "l2": f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
-                   "launch": f"CUDA graphs of {GRAPH_STEPS} steps each (programmatic launch between kernels)"},
+        "config": dict(workload_config(world),
+                       l2=f"{dec.R} rotating weight sets ({dec.R * 167} MB) > L2 (126 MB)",
+                       launch=f"CUDA graphs of {GRAPH_STEPS} steps each (programmatic launch between kernels)"),
         "tflops": world * step_flops / (ms_per_step * 1e9),
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
