@@ -370,7 +370,7 @@ def _rate(t, amount, scale):
 
 
 def decode_rows(fp8, torch, dec, hbm, out):
-    """Config 2 at every batch it names (M = 1, 16, 64): per layer the
+    """The decode linears at 1, 16 and 64 tokens: per layer the
     fp8_linear call (one kernel where the quantisation is fused, else
     act_quant + GEMM) and the whole three-layer step, over the same four
     rotating weight sets as the headline."""
@@ -492,7 +492,8 @@ def prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=False):
     # dense MLP, M = 4096: act_quant(x) -> w1|w3 -> silu*mul+act_quant -> w2.
     # ue8m0: every scale (weights and activations) a power of two, the GEMMs
     # on fp8_gemm_ue8m0 (the tensor core applies the block scales): the
-    # scale_fmt "ue8m0" reading extended to the weights, not config 3 itself
+    # scale_fmt "ue8m0" reading extended to the weights, not the fp32-scaled
+    # dense MLP workload itself
     M, D, I = 4096, syn.MLP_DIM, syn.MLP_INTER
     fmt = fp8.FP8_SCALE_UE8M0 if ue8m0 else fp8.FP8_SCALE_FP32
     gemm = fp8.fp8_gemm_ue8m0 if ue8m0 else fp8.fp8_gemm
@@ -528,7 +529,7 @@ def prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=False):
     del g
     if ue8m0:
         what = ("dense MLP M=4096, 7168->2x18432->7168, ue8m0 scales on weights and activations, "
-                "fp8_gemm_ue8m0 (outside config 3, whose weights carry fp32 scales): act_quant, w1|w3, "
+                "fp8_gemm_ue8m0 (not the fp32-scaled workload): act_quant, w1|w3, "
                 "silu*mul+act_quant, w2")
         row = {"workload": what, **unfused}
     else:
@@ -550,7 +551,7 @@ def prefill_row(fp8, torch, dev, fp8_peak, fp8_peak_sus, out, ue8m0=False):
         fused["gemm_swiglu"] = {"ms": tt["median"], "TFLOP/s": r["median"], "frac_fp8_peak": r["median"] / fp8_peak,
                                 "frac_fp8_peak_sustained": r["median"] / fp8_peak_sus}
         del gsw, w13i, s13i
-        what = ("dense MLP M=4096, 7168->2x18432->7168, fp32 scales (config 3): act_quant, fp8_gemm w1|w3 "
+        what = ("dense MLP M=4096, 7168->2x18432->7168, fp32 scales: act_quant, fp8_gemm w1|w3 "
                 "(bf16 h), fp8_silu_mul_quant, fp8_gemm w2")
         # the fused form (fp8_gemm_swiglu: no h in HBM) is reported beside it:
         # bit-identical, and slower -- its gate runs on the warps the tensor
