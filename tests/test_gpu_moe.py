@@ -23,8 +23,10 @@ def fp8():
 
 # T*topk % 4 == 0 takes the 16-byte-load path of the kernel (ragged warp
 # ranges included: 4093*8, 1000*2), the others the one-id-per-lane path
+# expert groups per CTA: 32 of 32 experts at E = 1024, one CTA at E = 1, a
+# last group of one expert at E = 33
 @pytest.mark.parametrize("T,E,topk", [(4096, 256, 8), (4093, 256, 8), (1000, 8, 2), (300, 16, 4), (1, 8, 2),
-                                      (37, 64, 6)])
+                                      (37, 64, 6), (2000, 1024, 8), (50, 1, 1), (777, 33, 5)])
 def test_route_matches_oracle_exactly(fp8, T, E, topk):
     rt = syn.moe_routing(T=T, E=E, topk=topk, seed=T + E)
     off, pr, rtok = fp8.fp8_moe_route(dev_i32(rt.ids), E)
