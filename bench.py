@@ -737,6 +737,21 @@ def _ncu_gemm(fp8, torch, M, N, K, ue8m0=False):
     fp8.fp8_device_status()
 
 
+def _ncu_swiglu(fp8, torch, M, I, K):
+    # fp8_gemm_swiglu on random codes (the weight rows taken as already
+    # interleaved): w1|w3 with the gate on warps 2-3
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7)
+    a = _ncu_rand_e4m3(torch, (M, K), gen)
+    w = _ncu_rand_e4m3(torch, (2 * I, K), gen)
+    a_s = torch.rand((M, K // 128), device="cuda", generator=gen) + 0.5
+    w_s = torch.rand((2 * I // 128, K // 128), device="cuda", generator=gen) + 0.5
+    for _ in range(3):
+        fp8.fp8_gemm_swiglu(a, a_s, w, w_s)
+    torch.cuda.synchronize()
+    fp8.fp8_device_status()
+
+
 def _ncu_linear(fp8, torch, M, N, K):
     x = syn.normal_bf16_device((M, K), 1.0, 11, "cuda", outlier_frac=0.005, outlier_mult=30.0)
     w, w_s = fp8.fp8_weight_quant(syn.normal_bf16_device((N, K), 0.02, 12, "cuda"))
@@ -792,6 +807,7 @@ NCU_CASES = {
     "prefill_w13": lambda fp8, torch: _ncu_gemm(fp8, torch, 4096, 2 * syn.MLP_INTER, syn.MLP_DIM),
     "prefill_w13_ue8m0": lambda fp8, torch: _ncu_gemm(fp8, torch, 4096, 2 * syn.MLP_INTER, syn.MLP_DIM,
                                                       ue8m0=True),
+    "prefill_w13_swiglu": lambda fp8, torch: _ncu_swiglu(fp8, torch, 4096, syn.MLP_INTER, syn.MLP_DIM),
     "act_quant": _ncu_act_quant,
     "weight_dequant": _ncu_dequant,
 }
